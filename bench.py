@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of the int4 group-128 weight-only decode path on one GB300.
+
+Step (what one timed iteration is): one synthetic decode step -- 36 layers x
+{fused qkv+gate+up 25,088x3072, o-proj 3072x3072, down 3072x8192} -- plus the
+wide output head (65,536x3072) and the argmax over its logits, all int4
+group-128 with fp16 scale/min, batch 1, replayed as one CUDA graph (the
+rumik-oss-1 page, "Step 3": 108 projections and the audio head in one CUDA
+graph).  Every step streams 2.243 GB of weights, far above the 129 MB L2, so
+no L2 flush is needed between steps.
+
+Metric: achieved HBM GB/s of algorithmic bytes (weights + activations +
+outputs) per step, plus decode-step microseconds at batch 1 and 8.  The
+dominant kernel's roofline is measured on the fused 25,088x3072 GEMV launched
+alone over 8 rotating weight copies (328 MB, so every launch reads DRAM).
+
+`--impl reference` times the fp64 CPU oracle on the same workload (a bounded
+sample of its matrices), in GB/s of the same algorithmic bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+LAYERS = synthetic.LAYERS
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SRC = os.path.join(ROOT, "int4_weight_only_q4_gb300", "csrc", "q4_gemv.cu")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algo_bytes(N: int, K: int, B: int) -> int:
+    """Codes + fp16 scale and min + bf16 activations in + fp32 outputs."""
+    return N * K // 2 + 4 * N * (K // 128) + 2 * B * K + 4 * B * N
+
+
+def step_shapes():
+    shapes = []
+    for _ in range(LAYERS):
+        for p in synthetic.LAYER_PROJS:
+            N, K, _ = synthetic.SHAPES[p]
+            shapes.append((N, K))
+    N, K, _ = synthetic.SHAPES["head"]
+    shapes.append((N, K))
+    return shapes
+
+
+def step_bytes(B: int) -> int:
+    return sum(algo_bytes(N, K, B) for N, K in step_shapes()) + 4 * B  # + argmax indices
+
+
+# ----------------------------------------------------------------------------- input generation
+def _gen_packed(job):
+    """Worker: one seeded matrix, packed by the library's host packer."""
+    kind, layer, proj, seed = job
+    sys.path.insert(0, ROOT)
+    import synthetic as S
+    from int4_weight_only_q4_gb300 import pack_host
+    if kind == "layer":
+        w, _ = S.decode_step_matrix(layer, proj, 1, seed)
+    else:
+        N, K, outl = S.SHAPES["head"]
+        w, _ = S.weights(N, K, seed + 1000, outl)
+    return pack_host(w, n_threads=2)
+
+
+def step_jobs(seed: int):
+    jobs = [("layer", l, p, seed) for l in range(LAYERS) for p in range(3)]
+    jobs.append(("head", 0, 0, seed))
+    return jobs
+
+
+def step_activations(B: int, seed: int):
+    """Activations of every matrix of the step, as bf16 bits [B, K]."""
+    rng = np.random.default_rng(seed + 7919 * B)
+    return [synthetic.f32_to_bf16_bits(rng.standard_normal((B, K), dtype=np.float32))
+            for _, K in step_shapes()]
+
+
+def generate_packed(seed: int, procs: int):
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(procs) as pool:
+        return pool.map(_gen_packed, step_jobs(seed), chunksize=1)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = max(smax, float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        loaded = [s for s in sm if s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peak_gbs():
+    try:
+        d = json.load(open(PEAKS_FILE))
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_src_sha() -> str:
+    h = hashlib.sha256()
+    for f in (KERNEL_SRC,):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the fused GEMV from the committed ncu summary, if still current."""
+    try:
+        d = json.load(open(TRAFFIC_FILE))
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_src_sha") != kernel_src_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- the oracle arm
+class OracleSampler:
+    """Times the fp64 CPU oracle (dequantise-then-matvec) on a bounded sample of the step:
+    row chunks of layer 0's three projections and of the head, in turn."""
+
+    CHUNK = 512
+    ROWS = 4096
+
+    def __init__(self, B: int = 1, seed: int = 0):
+        import oracle
+        self.oracle = oracle
+        ws = [synthetic.decode_step_matrix(0, p, 1, seed)[0] for p in range(3)]
+        N, K, outl = synthetic.SHAPES["head"]
+        ws.append(synthetic.weights(N, K, seed + 1000, outl)[0])
+        # the oracle's own quantiser prepares its inputs (untimed): the first ROWS rows of each
+        self.mats = [oracle.quantise_pack(np.ascontiguousarray(w[:self.ROWS])) for w in ws]
+        del ws
+        xs = step_activations(B, seed)
+        self.xs = [xs[0], xs[1], xs[2], xs[-1]]
+        self.B = B
+        self.pos = [0, 0, 0, 0]
+        self.m = 0
+
+    def run(self, seconds: float):
+        done, t_work, chunks = 0, 0.0, 0
+        while t_work < seconds or chunks == 0:
+            codes, sc, mn = self.mats[self.m]
+            N, H = codes.shape
+            K = 2 * H
+            r0 = self.pos[self.m]
+            rows = np.arange(r0, min(N, r0 + self.CHUNK))
+            t0 = time.perf_counter()
+            self.oracle.gemv_packed(codes, sc, mn, self.xs[self.m], rows=rows)
+            t_work += time.perf_counter() - t0
+            r = rows.size
+            done += r * (K // 2 + 4 * (K // 128) + 4 * self.B) + 2 * self.B * K * r // N
+            self.pos[self.m] = 0 if r0 + r >= N else r0 + r
+            self.m = (self.m + 1) % len(self.mats)
+            chunks += 1
+        return done, t_work, chunks
+
+    def describe(self, done, t_work, chunks):
+        return (f"{chunks} chunks of {self.CHUNK} rows from the first {self.ROWS} rows of layer-0 "
+                f"fused/o/down and the head, "
+                f"fp64 dequantise + matvec, B={self.B}: {done / 1e6:.1f} MB algorithmic in {t_work:.2f} s")
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    sampler = OracleSampler(1, args.seed)
+    budget = min(2.0, max(0.01, 150.0 / max(1, args.steps + args.warmup)))
+    per_step, tot = [], [0, 0.0, 0]
+    for i in range(args.warmup + args.steps):
+        done, t, c = sampler.run(budget)
+        if i >= args.warmup:
+            per_step.append(done / t / 1e9)
+            tot = [tot[0] + done, tot[1] + t, tot[2] + c]
+    value = statistics.median(per_step) if per_step else None
+    sb = step_bytes(1)
+    line = {
+        "impl": "reference", "metric": "int4 GEMV achieved HBM GB/s (decode step, B=1)", "value": value,
+        "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": (sb / (value * 1e9) * 1e3) if value else None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(1),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "per step: " + sampler.describe(*tot)},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def _config(B):
+    return {"workload": "decode step: 36 x {fused qkv+gate+up 25088x3072, o-proj 3072x3072, down 3072x8192} "
+                        "+ head 65536x3072 + argmax, int4 group-128 fp16 scale/min, one CUDA graph",
+            "batch": B, "seed": 0,
+            "l2": "inputs larger than L2 (2.24 GB of weights per step vs 129 MB L2); no flush",
+            "parallelism": "replicas (one independent step per GPU)"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    world, rank, local = dist_setup()
+    if args.gpus > 1 and world == 1:
+        print(json.dumps({"error": "launch with torchrun for --gpus > 1"}))
+        return 2
+    # CPU work that needs no GPU first (spawned pool: no CUDA state to inherit)
+    procs = max(1, min(16, (os.cpu_count() or 2)))
+    t0 = time.time()
+    packed = generate_packed(args.seed, procs)
+    gen_s = time.time() - t0
+
+    import torch
+    import int4_weight_only_q4_gb300 as q4
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    shapes = step_shapes()
+    mats = [q4.QuantizedMatrix.from_packed(*p, device=dev) for p in packed]
+    head_i = len(mats) - 1
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    graphs = {}
+    for B in (1, 8):
+        xs = step_activations(B, args.seed)
+        g = q4.DecodeStepGraph(mats, B, device=dev, with_argmax_of=head_i)
+        for i, x in enumerate(xs):
+            g.X[i].copy_(bf16(x))
+        graphs[B] = (g, xs)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def time_graph(g, steps, warmup):
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(steps):
+            g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        barrier()
+        return s.elapsed_time(e) / steps  # ms
+
+    g1, xs1 = graphs[1]
+    with ClockSampler(dev.index) as clk:
+        ms1 = time_graph(g1, args.steps, args.warmup)
+        # keep the GPU busy long enough for the clock sampler to see the load
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            time_graph(g1, 200, 0)
+    clocks = clk.summary()
+    ms1_t = torch.tensor([ms1], device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(ms1_t, op=dist.ReduceOp.MAX)
+    ms1 = float(ms1_t.item())
+    ms8 = time_graph(graphs[8][0], max(20, args.steps // 4), max(3, args.warmup))
+    sb1 = step_bytes(1)
+    value = sb1 * world / (ms1 * 1e-3) / 1e9
+
+    # decode step alone (108 projections, no head), batch 1 and 8: the metric's step time
+    dec_us = {}
+    for B in (1, 8):
+        gd = q4.DecodeStepGraph(mats[:head_i], B, device=dev)
+        for i, x in enumerate(graphs[B][1][:head_i]):
+            gd.X[i].copy_(bf16(x))
+        dec_us[f"b{B}"] = round(1e3 * time_graph(gd, max(50, args.steps // 4), max(3, args.warmup)), 2)
+        del gd
+
+    # dominant kernel: fused 25,088x3072 GEMV, 8 rotating copies, events per launch
+    roof = fused_roofline(q4, torch, mats[0], dev, args)
+
+    # end to end through the public API with pinned host buffers
+    e2e = end_to_end(q4, torch, g1, xs1, dev, max(10, args.steps // 20), barrier)
+
+    peak, src = measured_peak_gbs()
+    launches_per_step = len(mats) + 1
+    line = {
+        "metric": "int4 GEMV achieved HBM GB/s (decode step, B=1)", "value": round(value, 1), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms1, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4*bf16->f32",
+        "data": "synthetic", "config": _config(1), "clocks": clocks,
+        "frac_of_hbm_peak": round(value / world / peak, 4), "peak_source": src,
+        "decode_step_us": dec_us, "step_with_head_us": {"b1": round(ms1 * 1e3, 2), "b8": round(ms8 * 1e3, 2)},
+        "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof, "gen_seconds": round(gen_s, 1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sampler = OracleSampler(1, args.seed)
+        done, t, c = sampler.run(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(done / t / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": sampler.describe(done, t, c)}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def fused_roofline(q4, torch, W0, dev, args):
+    """Fused 25,088x3072 B=1 GEMV over 8 rotating weight copies; CUDA events around every launch."""
+    copies = []
+    for i in range(8):
+        copies.append(q4.QuantizedMatrix(W0.codes.clone(), W0.scales.clone(), W0.mins.clone(), W0.N, W0.K))
+    x = torch.randn((1, W0.K), device=dev).to(torch.bfloat16)
+    y = torch.empty((1, W0.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    n = max(64, args.steps // 4)
+    for i in range(16):
+        q4.gemm_skinny(copies[i % 8], x, y, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        evs[i][0].record(stream)
+        q4.gemm_skinny(copies[i % 8], x, y, stream=stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    durs = [a.elapsed_time(b) for a, b in evs]
+    avg_ms = sum(durs) / len(durs)
+    bytes_launch = algo_bytes(W0.N, W0.K, 1)
+    achieved = bytes_launch / (avg_ms * 1e-3) / 1e9
+    peak, src = measured_peak_gbs()
+    return {"bound": "hbm", "kernel": "q4_gemv_kernel (fused 25088x3072, B=1)", "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+            "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": round(avg_ms * 1e3, 3),
+            "median_launch_us": round(1e3 * statistics.median(durs), 3), "peak_source": src}
+
+
+def end_to_end(q4, torch, g, xs, dev, steps, barrier):
+    """Host->device activations, graph replay, device->host outputs + argmax, through the public API."""
+    hx = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs]
+    hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in g.Y]
+    hidx = torch.empty(g.idx.shape, dtype=g.idx.dtype).pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in hx)
+    bo = sum(t.numel() * t.element_size() for t in hy) + hidx.numel() * 4
+    for _ in range(3):
+        g.run_host(hx, hy, hidx)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        g.run_host(hx, hy, hidx)
+    dt = (time.perf_counter() - t0) / steps
+    value = step_bytes(g.B) / dt / 1e9
+    return {"value": round(value, 1), "unit": "GB/s", "ms_per_step": round(dt * 1e3, 4),
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

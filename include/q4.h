@@ -1,0 +1,171 @@
+/*
+ * q4.h -- C ABI of libq4.so: group-quantised int4 weight-only GEMV and skinny
+ * GEMM (batch 1..8) for small-batch autoregressive decoding on GB300 (sm_103a).
+ *
+ * Weight format (rumik-oss-1 int4 engine page, rtts.neoandmatrix.me,
+ * "Step 3: an int4 file and a first kernel"): every projection is quantised in
+ * groups of 128 consecutive columns of a row, with an fp16 scale and an fp16
+ * minimum per group and two 4-bit codes per byte; a weight is
+ *     w = code * scale + min.
+ *
+ * Canonical layout used by every call ("L0"):
+ *   W       logical [N, K]: output row n, input column k.  K % 128 == 0.
+ *   codes   uint8  [N, K/2] row-major.  Byte n*(K/2) + j holds column 2j in
+ *           bits 0-3 (low nibble first) and column 2j+1 in bits 4-7.
+ *   scales  fp16 bit patterns (uint16) [N, K/128] row-major, group g = k/128.
+ *   mins    fp16 bit patterns (uint16) [N, K/128] row-major.
+ *   X       bf16 bit patterns (uint16) [B, K] row-major (batch row b is X + b*K).
+ *   Y       fp32 [B, N] row-major (batch row b is the slice Y + b*N).
+ *
+ * Conventions for every device call below:
+ *   - Pointers marked "device" must be device (or managed) memory of the
+ *     current CUDA device.  The caller owns every buffer; the library never
+ *     allocates, frees or synchronises.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; a Q4_OK return means the
+ *     launch was accepted, not that it finished.
+ *   - Arguments are validated on the host before anything is enqueued; on an
+ *     error nothing is launched.  Launch failures are reported as Q4_ERR_CUDA.
+ *   - Every output column b of a call with batch B is bit-identical to the
+ *     output of the same call with B = 1 on that activation row alone
+ *     ("batch invariance", the pure-C TTS engine page, wpnews.pro, section
+ *     on the batched matvec that first accumulated in a different order).
+ *   - Calls are stateless apart from the caller's workspace and may be
+ *     issued from several host threads on different streams.
+ */
+#ifndef Q4_H
+#define Q4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    Q4_OK = 0,
+    Q4_ERR_INVALID_ARG = 1,        /* null pointer, N <= 0, B outside 1..8, non-finite weight, fp16 range */
+    Q4_ERR_UNSUPPORTED_SHAPE = 2,  /* K not a positive multiple of 128, or K > 65536, or N >= 2^31 */
+    Q4_ERR_MISALIGNED = 3,         /* codes/X/workspace not 16-byte aligned, Y not 4, scales/mins not 2 */
+    Q4_ERR_WORKSPACE = 4,          /* workspace missing or smaller than q4_workspace_bytes() */
+    Q4_ERR_CUDA = 5,               /* a CUDA runtime call or kernel launch failed */
+    Q4_ERR_TIMEOUT = 6             /* reserved: a bounded device-side wait gave up */
+} q4_status;
+
+/* One quantised matrix in layout L0.  All three arrays are device memory. */
+typedef struct {
+    const uint8_t*  codes;   /* [N, K/2] */
+    const uint16_t* scales;  /* [N, K/128] fp16 bits */
+    const uint16_t* mins;    /* [N, K/128] fp16 bits */
+    int64_t N;
+    int64_t K;
+} q4_matrix;
+
+/* How a call on an (N, K) matrix is split across the GPU.  Depends on N, K
+ * and the device's SM count only -- never on the batch size B. */
+typedef struct {
+    int32_t row_blocks;      /* CTAs along N */
+    int32_t k_splits;        /* CTAs along K (> 1: partial sums through the workspace) */
+    int32_t warps_per_cta;
+    int32_t prefetch_depth;  /* groups of codes in flight per warp */
+    int32_t kernel;          /* 0 = tensor-core (mma.sync bf16) dot, 1 = CUDA-core fp32 dot */
+    int32_t sm_count;
+} q4_plan_info;
+
+/*
+ * q4_pack_host -- the offline export job ("Step 3": a short CPU job exported
+ * the weights to a plain int4 format).  Host memory only.
+ *   w       host fp32 [N, K] row-major, finite.
+ *   codes   host out uint8 [N, K/2]; scales, mins host out uint16 [N, K/128].
+ *   n_threads  worker threads (<= 0: all hardware threads).
+ * Per row and per group of 128 columns: mn = min, mx = max (in double);
+ * scale = fp16((mx - mn) / 15) and min = fp16(mn), each rounded once from
+ * double to nearest-even; code = clamp(rint((w - min) / scale), 0, 15) in
+ * double with the stored fp16 scale/min (code 0 when scale == 0).
+ * Returns Q4_ERR_INVALID_ARG for null pointers, N <= 0, a non-finite weight,
+ * or a group whose scale or min overflows fp16 (outputs then undefined);
+ * Q4_ERR_UNSUPPORTED_SHAPE if K is not a positive multiple of 128.
+ */
+q4_status q4_pack_host(const float* w, int64_t N, int64_t K,
+                       uint8_t* codes, uint16_t* scales, uint16_t* mins,
+                       int n_threads);
+
+/*
+ * q4_workspace_bytes -- device workspace a q4_gemv / q4_gemm_skinny call on
+ * (N, K, B) needs on the current device (0 when the plan does not split K).
+ * The workspace holds fp32 partial sums and arrival counters.  It must be
+ * zero-filled once before its first use; every call leaves its counters at
+ * zero again when it completes, so the same buffer can be reused by later
+ * calls on the same stream (and by graph replays) without clearing.
+ * Returns 0 for invalid shapes.
+ */
+size_t q4_workspace_bytes(int64_t N, int64_t K, int B);
+
+/* q4_plan -- fill `out` with the split q4_gemv would use for (N, K) on the
+ * current device.  Host only; Q4_ERR_UNSUPPORTED_SHAPE / Q4_ERR_INVALID_ARG
+ * as for q4_gemv. */
+q4_status q4_plan(int64_t N, int64_t K, q4_plan_info* out);
+
+/*
+ * q4_gemv -- y = W x for one activation vector ("Step 3": the GEMV that
+ * dominates batch-1 decoding; fp32 accumulation).
+ *   W     host pointer to a q4_matrix whose arrays are device memory.
+ *   x     device bf16 bits [K], 16-byte aligned.
+ *   y     device fp32 [N], 4-byte aligned; fully overwritten.
+ *   ws    device workspace of ws_bytes >= q4_workspace_bytes(N, K, 1), or
+ *         NULL when that is 0.
+ * Same as q4_gemm_skinny with B = 1.
+ */
+q4_status q4_gemv(const q4_matrix* W, const uint16_t* x, float* y,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * q4_gemm_skinny -- Y[b, :] = W X[b, :] for b < B, 1 <= B <= 8 (the pure-C TTS
+ * engine page's continuous batching: every weight row is read once and reused
+ * for all B activation rows).  Column b of Y is bit-identical to q4_gemv on
+ * X[b, :] alone.
+ *   X  device bf16 bits [B, K] (16-byte aligned);  Y  device fp32 [B, N].
+ *   ws as for q4_gemv with q4_workspace_bytes(N, K, B).
+ */
+q4_status q4_gemm_skinny(const q4_matrix* W, const uint16_t* X, int B, float* Y,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * q4_decode_step -- the weight-streaming part of one decode step: n_mats
+ * independent skinny GEMMs enqueued back to back on `stream`, in list order
+ * ("Step 3": 108 projections of 36 layers in one CUDA graph; "Step 4": q, k,
+ * v, gate and up fused into one 25,088-row matrix, three GEMVs per layer).
+ *   mats  host array [n_mats] of q4_matrix (device arrays inside).
+ *   X     host array [n_mats] of device bf16 pointers, X[i] is [B, mats[i].K].
+ *   Y     host array [n_mats] of device fp32 pointers, Y[i] is [B, mats[i].N].
+ *   ws    one workspace of at least max_i q4_workspace_bytes(N_i, K_i, B);
+ *         the launches are stream-ordered, so they share it.
+ * Each launch lets the next one start streaming its (read-only) weights
+ * before the previous one has finished (programmatic dependent launch); a
+ * launch reads X[i] and writes Y[i] only after every earlier launch in the
+ * stream has completed, so Y[i] may feed X[j] for j > i.  The host arrays are
+ * consumed before the call returns, so the call can be captured into a CUDA
+ * graph and replayed.  Validates every matrix before launching any.
+ */
+q4_status q4_decode_step(const q4_matrix* mats, int n_mats,
+                         const uint16_t* const* X, float* const* Y, int B,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * q4_argmax_f32 -- per batch row of logits Y [B, N] (device fp32), the index
+ * of the largest value, the lowest index among equal maxima (NaN ranks above
+ * every number, as numpy's argmax does), written to idx (device int32 [B]).
+ * The greedy pick after the output head ("Step 4" of the rumik-oss-1 page
+ * samples on the GPU; argmax is its deterministic case).
+ * Q4_ERR_INVALID_ARG for null pointers, B outside 1..8 or N outside 1..2^31-1.
+ */
+q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* q4_status_string(q4_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q4_H */

@@ -1,0 +1,325 @@
+"""GPU parity of libq4.so against the fp64 CPU oracle.
+
+Tolerance: the stated bound, max relative error <= 2e-3 per output with a floor
+of 1% of the output RMS for outputs near zero (fp32 accumulation on the GPU,
+fp64 on the oracle).  Packing and argmax are compared exactly; each batch
+column of the skinny GEMM is compared bit for bit with the batch-1 GEMV (the
+pure-C TTS engine page, wpnews.pro: batched output must equal single-stream
+output).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import synthetic
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def q4():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import int4_weight_only_q4_gb300 as m
+    return m
+
+
+def bf16_tensor(x_bits: np.ndarray) -> "torch.Tensor":
+    return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def oracle_rows(w, x_bits, rows=None, chunk=8192):
+    """Oracle output for the given rows (quantising only those rows, a chunk at a time)."""
+    idx = np.arange(w.shape[0]) if rows is None else np.asarray(rows)
+    out = []
+    for s in range(0, idx.size, chunk):
+        p, sb, mb = oracle.quantise_pack(np.ascontiguousarray(w[idx[s:s + chunk]]))
+        out.append(oracle.gemv_packed(p, sb, mb, x_bits))
+    return np.concatenate(out, axis=1)
+
+
+def run(q4, W, x_bits, ws=None):
+    X = bf16_tensor(x_bits)
+    Y = q4.gemm_skinny(W, X, workspace=ws)
+    torch.cuda.synchronize()
+    return Y.cpu().numpy()
+
+
+# ----------------------------------------------------------------------------- small configs
+def test_tiny_config_b1(q4):
+    w, x = synthetic.problem("tiny", 1, seed=0)
+    W = q4.QuantizedMatrix.from_float(w)
+    y = run(q4, W, x)
+    assert oracle.rel_err(y, oracle_rows(w, x)) <= TOL
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 128), (16, 256), (17, 384), (33, 512), (100, 1152),
+                                 (1000, 640), (4099, 1024), (257, 8192), (40, 16384)])
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_odd_shapes(q4, N, K, B):
+    w, x = synthetic.random_shape_problem(N, K, B, seed=N * 7 + K + B, outliers=True)
+    W = q4.QuantizedMatrix.from_float(w)
+    y = run(q4, W, x)
+    assert oracle.rel_err(y, oracle_rows(w, x)) <= TOL
+
+
+def test_gemv_entry_point_equals_skinny_b1(q4):
+    w, x = synthetic.random_shape_problem(300, 1024, 1, seed=3)
+    W = q4.QuantizedMatrix.from_float(w)
+    X = bf16_tensor(x)
+    y1 = q4.gemv(W, X[0])
+    y2 = q4.gemm_skinny(W, X)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2[0])
+
+
+def test_known_answer_gemv_through_gpu(q4):
+    import json, os
+    fx = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "known_answers.json")))
+    groups = {g["name"]: g for g in fx["groups"]}
+    for case in fx["gemv"]:
+        w = np.array([groups[r]["w"] for r in case["rows"]], np.float32)
+        K = w.shape[1]
+        xf = np.ones(K, np.float32) if case["x"] == "ones" else \
+            np.array([1.0 if k % 2 == 0 else -1.0 for k in range(K)], np.float32)
+        W = q4.QuantizedMatrix.from_float(w)
+        y = run(q4, W, synthetic.f32_to_bf16_bits(xf)[None, :])[0]
+        assert np.allclose(y, case["y"], rtol=1e-6, atol=1e-6), case["name"]
+
+
+def test_closed_forms_on_gpu(q4):
+    """All-zero codes leave sum_g min_g * S_g; a one-hot x picks one dequantised column."""
+    N, K = 64, 512
+    w, x = synthetic.random_shape_problem(N, K, 2, seed=8)
+    c, s, m = q4.pack_host(w)
+    Wz = q4.QuantizedMatrix.from_packed(np.zeros_like(c), s, m)
+    y = run(q4, Wz, x)
+    S = oracle.bf16_bits_to_f64(x).reshape(2, K // 128, 128).sum(2)
+    assert oracle.rel_err(y, S @ oracle.f16_bits_to_f64(m).T) <= TOL
+    W = q4.QuantizedMatrix.from_packed(c, s, m)
+    w_hat = oracle.dequantise(oracle.unpack(c), s, m)
+    for k in (0, 1, 2, 5, 127, 128, 300, 511):
+        xh = np.zeros((1, K), np.uint16)
+        xh[0, k] = 0x3F80
+        yk = run(q4, W, xh)[0]
+        assert np.allclose(yk, w_hat[:, k], rtol=1e-6, atol=1e-7), k
+
+
+# ----------------------------------------------------------------------------- batch invariance
+@pytest.mark.parametrize("N,K", [(256, 512), (3072, 3072), (1000, 8192), (4099, 1024)])
+def test_batch_columns_bit_identical_to_b1(q4, N, K):
+    w, x = synthetic.random_shape_problem(N, K, 8, seed=N + K, outliers=True)
+    W = q4.QuantizedMatrix.from_float(w)
+    X = bf16_tensor(x)
+    singles = [q4.gemm_skinny(W, X[b:b + 1].contiguous()) for b in range(8)]
+    for B in (2, 4, 8, 5):
+        Y = q4.gemm_skinny(W, X[:B].contiguous())
+        for b in range(B):
+            assert torch.equal(Y[b], singles[b][0]), (B, b)
+    perm = torch.tensor([5, 2, 7, 0, 1, 6, 3, 4], device="cuda")
+    Yp = q4.gemm_skinny(W, X[perm].contiguous())
+    for i, b in enumerate(perm.tolist()):
+        assert torch.equal(Yp[i], singles[b][0])
+    torch.cuda.synchronize()
+
+
+def test_k_split_path_parity_and_invariance(q4, monkeypatch):
+    monkeypatch.setenv("Q4_KSPLIT", "3")
+    N, K = 3072, 3072
+    assert q4.plan(N, K)["k_splits"] == 3
+    w, x = synthetic.random_shape_problem(N, K, 8, seed=77, outliers=True)
+    W = q4.QuantizedMatrix.from_float(w)
+    ws = q4.Workspace(q4.workspace_bytes(N, K, 8))
+    X = bf16_tensor(x)
+    Y8 = q4.gemm_skinny(W, X, workspace=ws)
+    Y8b = q4.gemm_skinny(W, X, workspace=ws)          # counters were reset by the first call
+    for b in range(8):
+        y1 = q4.gemm_skinny(W, X[b:b + 1].contiguous(), workspace=ws)
+        assert torch.equal(Y8[b], y1[0])
+    assert torch.equal(Y8, Y8b)
+    torch.cuda.synchronize()
+    assert oracle.rel_err(Y8.cpu().numpy(), oracle_rows(w, x)) <= TOL
+    assert int(ws.buf[:256].view(torch.int32)[: q4.plan(N, K)["row_blocks"]].abs().sum()) == 0
+
+
+@pytest.mark.parametrize("env", [{"Q4_KERNEL": "1"}, {"Q4_DEPTH": "2"}, {"Q4_DEPTH": "6"},
+                                 {"Q4_WARPS": "8", "Q4_DEPTH": "4"}, {"Q4_WARPS": "8", "Q4_DEPTH": "8"},
+                                 {"Q4_WARPS": "32", "Q4_DEPTH": "2"}, {"Q4_PDL": "0"},
+                                 {"Q4_L2_PREFETCH": "1048576"}])
+def test_kernel_variants(q4, monkeypatch, env):
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    for (N, K) in ((1000, 1152), (3072, 3072)):
+        w, x = synthetic.random_shape_problem(N, K, 8, seed=5, outliers=True)
+        W = q4.QuantizedMatrix.from_float(w)
+        X = bf16_tensor(x)
+        Y = q4.gemm_skinny(W, X)
+        y1 = q4.gemm_skinny(W, X[3:4].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(Y[3], y1[0])
+        assert oracle.rel_err(Y.cpu().numpy(), oracle_rows(w, x)) <= TOL
+
+
+# ----------------------------------------------------------------------------- full-size configs
+def _sample_rows(N, outl_rows=None, n=1024, seed=1):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(N, min(n, N), replace=False).tolist()) | {0, N - 1, N // 2}
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", ["fused", "oproj", "down"])
+@pytest.mark.parametrize("B", [1, 8])
+def test_full_size_projection_sampled_rows(q4, name, B):
+    w, x = synthetic.problem(name, B, seed=0)
+    W = q4.QuantizedMatrix.from_float(w)
+    y = run(q4, W, x)
+    rows = _sample_rows(w.shape[0])
+    assert oracle.rel_err(y[:, rows], oracle_rows(w, x, rows)) <= TOL
+    # packing of the sampled rows is bit-exact
+    c, s, m = (t.cpu().numpy() for t in (W.codes, W.scales.view(torch.int16), W.mins.view(torch.int16)))
+    oc, osb, omb = oracle.quantise(np.ascontiguousarray(w[rows]))
+    assert np.array_equal(c[rows], oracle.pack(oc))
+    assert np.array_equal(s[rows].view(np.uint16), osb) and np.array_equal(m[rows].view(np.uint16), omb)
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_head_and_argmax_exact(q4, B):
+    w, x = synthetic.problem("head", B, seed=0)
+    W = q4.QuantizedMatrix.from_float(w)
+    X = bf16_tensor(x)
+    Y = q4.gemm_skinny(W, X)
+    idx = q4.argmax(Y)
+    torch.cuda.synchronize()
+    y = Y.cpu().numpy()
+    # argmax kernel == numpy on the same fp32 logits (exact)
+    assert idx.cpu().numpy().tolist() == np.argmax(y, axis=1).tolist()
+    # oracle logits: full head in row chunks
+    y_ref = oracle_rows(w, x)
+    assert oracle.rel_err(y, y_ref) <= TOL
+    ref_idx = oracle.argmax_first(y_ref)
+    bound = 2.0 * float(np.abs(y - y_ref).max())     # either index is right inside the GPU's own error
+    for b in range(B):
+        if oracle.argmax_ambiguous(y_ref[b], bound):
+            assert y_ref[b, idx[b].item()] >= y_ref[b].max() - bound
+        else:
+            assert idx[b].item() == ref_idx[b]
+
+
+def test_argmax_ties_nan_and_layout(q4):
+    y = np.random.default_rng(0).standard_normal((8, 70001)).astype(np.float32)
+    y[0, 5] = y[0, 9] = 100.0               # tie: lowest index
+    y[1, :] = 0.0; y[1, 3] = -0.0           # all equal: index 0
+    y[2, 123] = np.nan; y[2, 7] = 1e30       # NaN ranks first (numpy convention)
+    y[3, -1] = 50.0                          # last element
+    y[4, :] = -np.inf; y[4, 17] = -1e38
+    Y = torch.from_numpy(y).cuda()
+    got = q4.argmax(Y).cpu().numpy()
+    assert got.tolist() == np.argmax(y, axis=1).tolist()
+    assert got[0] == 5 and got[1] == 0 and got[2] == 123 and got[3] == 70000 and got[4] == 17
+
+
+# ----------------------------------------------------------------------------- decode step
+def _decode_mats(q4, layers, B, base=0):
+    mats, xs, ws_np = [], [], []
+    for l in range(layers):
+        for p in range(3):
+            w, x = synthetic.decode_step_matrix(l, p, B, base)
+            mats.append(q4.QuantizedMatrix.from_float(w))
+            xs.append(x)
+            ws_np.append(w)
+    return mats, xs, ws_np
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_decode_step_graph_equals_eager_and_oracle(q4, B):
+    layers = 3
+    mats, xs, ws_np = _decode_mats(q4, layers, B)
+    g = q4.DecodeStepGraph(mats, B)
+    for i, x in enumerate(xs):
+        g.X[i].copy_(bf16_tensor(x))
+    g.replay()
+    g.replay()                                  # replays are repeatable
+    eager_Y = [torch.empty_like(y) for y in g.Y]
+    q4.decode_step(mats, g.X, eager_Y, g.ws)
+    torch.cuda.synchronize()
+    for i in range(len(mats)):
+        assert torch.equal(g.Y[i], eager_Y[i]), i
+        single = q4.gemm_skinny(mats[i], g.X[i])
+        assert torch.equal(single, eager_Y[i]), i
+    for i in range(len(mats)):
+        rows = _sample_rows(ws_np[i].shape[0], n=256, seed=i)
+        y = g.Y[i].cpu().numpy()
+        assert oracle.rel_err(y[:, rows], oracle_rows(ws_np[i], xs[i], rows)) <= TOL, i
+
+
+def test_decode_step_chained_dependency(q4):
+    """Y of one launch feeding X of the next is honoured (the launch waits for its producer)."""
+    w1, x1 = synthetic.random_shape_problem(1024, 1024, 1, seed=1)
+    w2, _ = synthetic.random_shape_problem(512, 1024, 1, seed=2)
+    W1, W2 = q4.QuantizedMatrix.from_float(w1), q4.QuantizedMatrix.from_float(w2)
+    X1 = bf16_tensor(x1)
+    Y1 = torch.empty((1, 1024), dtype=torch.float32, device="cuda")
+    X2 = torch.empty((1, 1024), dtype=torch.bfloat16, device="cuda")
+    Y2 = torch.empty((1, 512), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        q4.decode_step([W1], [X1], [Y1])
+        X2.copy_(Y1)                               # a torch kernel between the two launches
+        q4.decode_step([W2], [X2], [Y2])
+    torch.cuda.synchronize()
+    ref = q4.gemm_skinny(W2, Y1.to(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert torch.equal(ref, Y2)
+
+
+# ----------------------------------------------------------------------------- guard bands + errors
+def test_outputs_stay_inside_their_buffers(q4):
+    N, K, B = 1001, 640, 3
+    w, x = synthetic.random_shape_problem(N, K, B, seed=4)
+    W = q4.QuantizedMatrix.from_float(w)
+    pad = 1024
+    big = torch.full((B * N + 2 * pad,), 12345.0, dtype=torch.float32, device="cuda")
+    Y = big[pad:pad + B * N].view(B, N)
+    q4.gemm_skinny(W, bf16_tensor(x), Y=Y)
+    torch.cuda.synchronize()
+    assert bool((big[:pad] == 12345.0).all()) and bool((big[pad + B * N:] == 12345.0).all())
+    assert oracle.rel_err(Y.cpu().numpy(), oracle_rows(w, x)) <= TOL
+
+
+def test_error_statuses_on_device(q4, monkeypatch):
+    import ctypes
+    from int4_weight_only_q4_gb300 import _lib
+    w, x = synthetic.random_shape_problem(3072, 3072, 1, seed=1)
+    W = q4.QuantizedMatrix.from_float(w)
+    X = bf16_tensor(x)
+    Y = torch.empty((1, 3072), dtype=torch.float32, device="cuda")
+    m = W.c_struct()
+    L = _lib.lib
+    # misaligned x
+    assert L.q4_gemv(ctypes.byref(m), X.data_ptr() + 2, Y.data_ptr(), None, 0, None) == _lib.Q4_ERR_MISALIGNED
+    # workspace required but missing / too small under a forced k-split
+    monkeypatch.setenv("Q4_KSPLIT", "2")
+    need = q4.workspace_bytes(3072, 3072, 1)
+    assert need > 0
+    assert L.q4_gemv(ctypes.byref(m), X.data_ptr(), Y.data_ptr(), None, 0, None) == _lib.Q4_ERR_WORKSPACE
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    assert L.q4_gemv(ctypes.byref(m), X.data_ptr(), Y.data_ptr(), ws.data_ptr(), need - 16, None) == \
+        _lib.Q4_ERR_WORKSPACE
+    assert L.q4_gemv(ctypes.byref(m), X.data_ptr(), Y.data_ptr(), ws.data_ptr(), need, None) == _lib.Q4_OK
+    monkeypatch.delenv("Q4_KSPLIT")
+    # a simulated launch failure is reported, and nothing is launched
+    Y.fill_(7.0)
+    monkeypatch.setenv("Q4_FAULT_INJECT", "launch")
+    assert L.q4_gemv(ctypes.byref(m), X.data_ptr(), Y.data_ptr(), None, 0, None) == _lib.Q4_ERR_CUDA
+    with pytest.raises(q4.Q4Error):
+        q4.gemv(W, X[0], Y[0])
+    monkeypatch.delenv("Q4_FAULT_INJECT")
+    torch.cuda.synchronize()
+    assert bool((Y == 7.0).all())
+    # the context is healthy afterwards
+    y = q4.gemv(W, X[0])
+    torch.cuda.synchronize()
+    assert oracle.rel_err(y.cpu().numpy()[None], oracle_rows(w, x)) <= TOL
