@@ -10,9 +10,12 @@ graph).  Every step streams 2.243 GB of weights, far above the 129 MB L2, so
 no L2 flush is needed between steps.
 
 Metric: achieved HBM GB/s of algorithmic bytes (weights + activations +
-outputs) per step, plus decode-step microseconds at batch 1 and 8.  The
-dominant kernel's roofline is measured on the fused 25,088x3072 GEMV launched
-alone over 8 rotating weight copies (328 MB, so every launch reads DRAM).
+outputs) per step, plus decode-step microseconds at batch 1 and 8.  The step
+is three launches: activation prep, the persistent tile kernel over all 109
+matrices, argmax.  The dominant kernel's roofline is that tile kernel, timed
+alone with CUDA events around each launch (activations prepared once before).
+The fused 25,088x3072 GEMV is also timed as a single call over 8 rotating
+weight copies (328 MB, so every launch reads DRAM).
 
 `--impl reference` times the fp64 CPU oracle on the same workload (a bounded
 sample of its matrices), in GB/s of the same algorithmic bytes.
@@ -167,15 +170,16 @@ def kernel_src_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the fused GEMV from the committed ncu summary, if still current."""
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the kernel source is
+    unchanged since it was taken; else None."""
     try:
         d = json.load(open(TRAFFIC_FILE))
     except (OSError, ValueError):
         return None
     if d.get("kernel_src_sha") != kernel_src_sha():
         return None
-    return d.get("dram_bytes_per_launch")
+    return d.get("dram_bytes_per_launch", {}).get(kernel)
 
 
 def dist_setup():
@@ -344,32 +348,36 @@ def run_ours(args):
     sb1 = step_bytes(1)
     value = sb1 * world / (ms1 * 1e-3) / 1e9
 
-    # decode step alone (108 projections, no head), batch 1 and 8: the metric's step time
-    dec_us = {}
+    # decode step alone (108 projections, no head), batch 1 and 8: the metric's step time; the
+    # same step as 108 dependency-safe launches (one per matrix) for comparison
+    dec_us, chained_us = {}, {}
     for B in (1, 8):
-        gd = q4.DecodeStepGraph(mats[:head_i], B, device=dev)
-        for i, x in enumerate(graphs[B][1][:head_i]):
-            gd.X[i].copy_(bf16(x))
-        dec_us[f"b{B}"] = round(1e3 * time_graph(gd, max(50, args.steps // 4), max(3, args.warmup)), 2)
-        del gd
+        for indep, out in ((True, dec_us), (False, chained_us)):
+            gd = q4.DecodeStepGraph(mats[:head_i], B, device=dev, independent=indep)
+            for i, x in enumerate(graphs[B][1][:head_i]):
+                gd.X[i].copy_(bf16(x))
+            out[f"b{B}"] = round(1e3 * time_graph(gd, max(50, args.steps // 4), max(3, args.warmup)), 2)
+            del gd
 
-    # dominant kernel: fused 25,088x3072 GEMV, 8 rotating copies, events per launch
-    roof = fused_roofline(q4, torch, mats[0], dev, args)
+    # dominant kernel: the step's persistent tile kernel, events around every launch
+    roof = step_roofline(q4, torch, mats, graphs[1][0], dev, args)
+    # the single fused 25,088x3072 GEMV call, 8 rotating copies, events per launch
+    fused_single = fused_roofline(q4, torch, mats[0], dev, args)
 
     # end to end through the public API with pinned host buffers
     e2e = end_to_end(q4, torch, g1, xs1, dev, max(10, args.steps // 20), barrier)
 
     peak, src = measured_peak_gbs()
-    launches_per_step = len(mats) + 1
+    launches_per_step = 2 * ((len(mats) + 127) // 128) + 1  # prep + tile kernel per 128 matrices, argmax
     line = {
         "metric": "int4 GEMV achieved HBM GB/s (decode step, B=1)", "value": round(value, 1), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms1, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int4*bf16->f32",
         "data": "synthetic", "config": _config(1), "clocks": clocks,
         "frac_of_hbm_peak": round(value / world / peak, 4), "peak_source": src,
-        "decode_step_us": dec_us, "step_with_head_us": {"b1": round(ms1 * 1e3, 2), "b8": round(ms8 * 1e3, 2)},
+        "decode_step_us": dec_us, "decode_step_chained_launches_us": chained_us, "step_with_head_us": {"b1": round(ms1 * 1e3, 2), "b8": round(ms8 * 1e3, 2)},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-        "roofline": roof, "gen_seconds": round(gen_s, 1),
+        "roofline": roof, "fused_gemv_single_call": fused_single, "gen_seconds": round(gen_s, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sampler = OracleSampler(1, args.seed)
@@ -382,6 +390,34 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def step_roofline(q4, torch, mats, g, dev, args):
+    """The step's tile kernel (all 109 matrices, B=1) alone: activations prepared once, then
+    CUDA events around every q4_step_stream launch on the current stream."""
+    ws = q4.Workspace(q4.step_workspace_bytes([m.K for m in mats], 1))
+    stream = torch.cuda.current_stream()
+    q4.step_prepare(mats, g.X, ws, stream=stream)
+    n = max(20, args.steps // 10)
+    for _ in range(5):
+        q4.step_stream(mats, g.Y, 1, ws, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for i in range(n):
+        evs[i][0].record(stream)
+        q4.step_stream(mats, g.Y, 1, ws, stream=stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    durs = [a.elapsed_time(b) for a, b in evs]
+    avg_ms = sum(durs) / len(durs)
+    bytes_launch = sum(algo_bytes(N, K, 1) for N, K in step_shapes())
+    achieved = bytes_launch / (avg_ms * 1e-3) / 1e9
+    peak, src = measured_peak_gbs()
+    return {"bound": "hbm", "kernel": "q4_tiles_kernel (109 matrices of the step, B=1, one launch)",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic("q4_tiles_kernel"), "algorithmic_bytes_per_launch": bytes_launch,
+            "avg_launch_us": round(avg_ms * 1e3, 2), "median_launch_us": round(1e3 * statistics.median(durs), 2),
+            "peak_source": src}
 
 
 def fused_roofline(q4, torch, W0, dev, args):
@@ -407,8 +443,8 @@ def fused_roofline(q4, torch, W0, dev, args):
     bytes_launch = algo_bytes(W0.N, W0.K, 1)
     achieved = bytes_launch / (avg_ms * 1e-3) / 1e9
     peak, src = measured_peak_gbs()
-    return {"bound": "hbm", "kernel": "q4_gemv_kernel (fused 25088x3072, B=1)", "achieved": round(achieved, 1),
-            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+    return {"bound": "hbm", "kernel": "q4_direct_kernel (fused 25088x3072, B=1, single call)",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": round(avg_ms * 1e3, 3),
             "median_launch_us": round(1e3 * statistics.median(durs), 3), "peak_source": src}
 

@@ -50,16 +50,30 @@ typedef enum {
     Q4_ERR_MISALIGNED = 3,         /* codes/X/workspace not 16-byte aligned, Y not 4, scales/mins not 2 */
     Q4_ERR_WORKSPACE = 4,          /* workspace missing or smaller than q4_workspace_bytes() */
     Q4_ERR_CUDA = 5,               /* a CUDA runtime call or kernel launch failed */
-    Q4_ERR_TIMEOUT = 6             /* reserved: a bounded device-side wait gave up */
+    Q4_ERR_TIMEOUT = 6             /* a bounded device-side wait gave up (see q4_device_status) */
 } q4_status;
 
-/* One quantised matrix in layout L0.  All three arrays are device memory. */
+/*
+ * One quantised matrix, device memory.  Either or both of:
+ *   - the canonical layout L0 (codes, scales, mins; all three non-NULL), and
+ *   - a tiled copy (`tiled`, built by q4_tile from L0): the layout the default
+ *     kernels stream.  For each 16-row tile j (rows 16j..16j+15; rows >= N are
+ *     zero) and each 128-column group g, one 1,088-byte record at offset
+ *     (j * K/128 + g) * 1088:
+ *        bytes    0..511   for l = 0..31: L0 bytes g*64 + 16*(l%4) .. +15 of row 16j + l/4
+ *        bytes  512..1023  the same for row 16j + l/4 + 8
+ *        bytes 1024..1087  for q = 0..7: (scale | min << 16) of row 16j+q, then of row 16j+q+8
+ *     A warp reads one record with two 512-byte loads and one 64-byte load.
+ * A call uses the tiled copy when present (and the default kernel is selected),
+ * else L0.
+ */
 typedef struct {
-    const uint8_t*  codes;   /* [N, K/2] */
-    const uint16_t* scales;  /* [N, K/128] fp16 bits */
-    const uint16_t* mins;    /* [N, K/128] fp16 bits */
+    const uint8_t*  codes;   /* L0 [N, K/2], or NULL */
+    const uint16_t* scales;  /* L0 [N, K/128] fp16 bits, or NULL */
+    const uint16_t* mins;    /* L0 [N, K/128] fp16 bits, or NULL */
     int64_t N;
     int64_t K;
+    const void*     tiled;   /* tiled copy, q4_tiled_bytes(N, K) bytes, 16-byte aligned, or NULL */
 } q4_matrix;
 
 /* How a call on an (N, K) matrix is split across the GPU.  Depends on N, K
@@ -68,8 +82,13 @@ typedef struct {
     int32_t row_blocks;      /* CTAs along N */
     int32_t k_splits;        /* CTAs along K (> 1: partial sums through the workspace) */
     int32_t warps_per_cta;
-    int32_t prefetch_depth;  /* groups of codes in flight per warp */
-    int32_t kernel;          /* 0 = tensor-core (mma.sync bf16) dot, 1 = CUDA-core fp32 dot */
+    int32_t prefetch_depth;  /* direct kernel: groups in flight per warp; stream kernel: ring stages */
+    int32_t kernel;          /* 0 direct on the tiled copy + tensor-core dot (single matrices),
+                                1 direct on L0 + tensor-core dot, 2 direct on L0 + CUDA-core fp32 dot,
+                                3 stream (bulk copies into a shared-memory ring) on the tiled copy
+                                  + tensor-core dot, 4 direct on the tiled copy + CUDA-core fp32 dot,
+                                5 tile kernel: prepared activations + whole 16-row tiles per warp,
+                                  persistent over a list (independent lists of several matrices) */
     int32_t sm_count;
 } q4_plan_info;
 
@@ -90,6 +109,18 @@ typedef struct {
 q4_status q4_pack_host(const float* w, int64_t N, int64_t K,
                        uint8_t* codes, uint16_t* scales, uint16_t* mins,
                        int n_threads);
+
+/* Bytes of the tiled copy of an (N, K) matrix: ceil(N/16) * (K/128) * 1088 (0 if invalid). */
+size_t q4_tiled_bytes(int64_t N, int64_t K);
+
+/*
+ * q4_tile -- build the tiled copy of W's L0 arrays into `tiled` (device,
+ * 16-byte aligned, at least q4_tiled_bytes(N, K) bytes), asynchronously on
+ * `stream`.  A pure rearrangement: no value changes.  Q4_ERR_INVALID_ARG if
+ * W's L0 arrays or `tiled` are NULL, Q4_ERR_WORKSPACE if tiled_bytes is too
+ * small, Q4_ERR_MISALIGNED / Q4_ERR_UNSUPPORTED_SHAPE as for q4_gemv.
+ */
+q4_status q4_tile(const q4_matrix* W, void* tiled, size_t tiled_bytes, void* stream);
 
 /*
  * q4_workspace_bytes -- device workspace a q4_gemv / q4_gemm_skinny call on
@@ -131,26 +162,80 @@ q4_status q4_gemv(const q4_matrix* W, const uint16_t* x, float* y,
 q4_status q4_gemm_skinny(const q4_matrix* W, const uint16_t* X, int B, float* Y,
                          void* ws, size_t ws_bytes, void* stream);
 
+/* Flag of q4_decode_step: the matrices are independent (no X[j] overlaps any Y[i]). */
+#define Q4_STEP_INDEPENDENT 1u
+
 /*
- * q4_decode_step -- the weight-streaming part of one decode step: n_mats
- * independent skinny GEMMs enqueued back to back on `stream`, in list order
- * ("Step 3": 108 projections of 36 layers in one CUDA graph; "Step 4": q, k,
- * v, gate and up fused into one 25,088-row matrix, three GEMVs per layer).
+ * q4_decode_step -- the weight-streaming part of one decode step: n_mats skinny
+ * GEMMs Y[i] = mats[i] X[i] in list order ("Step 3": 108 projections of 36
+ * layers in one CUDA graph; "Step 4": q, k, v, gate and up fused into one
+ * 25,088-row matrix, three GEMVs per layer).
  *   mats  host array [n_mats] of q4_matrix (device arrays inside).
  *   X     host array [n_mats] of device bf16 pointers, X[i] is [B, mats[i].K].
  *   Y     host array [n_mats] of device fp32 pointers, Y[i] is [B, mats[i].N].
- *   ws    one workspace of at least max_i q4_workspace_bytes(N_i, K_i, B);
- *         the launches are stream-ordered, so they share it.
- * Each launch lets the next one start streaming its (read-only) weights
- * before the previous one has finished (programmatic dependent launch); a
- * launch reads X[i] and writes Y[i] only after every earlier launch in the
- * stream has completed, so Y[i] may feed X[j] for j > i.  The host arrays are
- * consumed before the call returns, so the call can be captured into a CUDA
- * graph and replayed.  Validates every matrix before launching any.
+ *   ws    workspace of at least q4_decode_step_workspace_bytes(...) for the
+ *         same shapes, B and flags (zero-filled once before first use).
+ *   flags Q4_STEP_INDEPENDENT: the caller guarantees that no X[j] overlaps any
+ *         Y[i]; the whole list then runs as ONE persistent launch (at most 128
+ *         matrices per launch) in which every SM walks the list in order and
+ *         starts streaming the next matrix's weights while finishing the
+ *         previous one (the rumik-oss-1 page's H100 lesson: at ~230 launches
+ *         per step the fixed cost per kernel, not the bytes, set the speed).
+ *         0: one launch per matrix; launch i+1 may start streaming its
+ *         weights early but reads X[i+1] and writes Y[i+1] only after launch i
+ *         has completed, so Y[i] may feed X[j] for j > i.
+ * Kernels: an independent list of more than one matrix whose matrices all carry
+ * the tiled copy runs as q4_step_prepare + q4_step_stream (two launches per 128
+ * matrices).  Otherwise each matrix runs as q4_gemm_skinny does.  The two add
+ * the 128-column groups of a row in different fixed orders (all groups in
+ * sequence, versus K split across the warps of a CTA), so their outputs agree
+ * to fp32 rounding, not bit for bit; each is bit-identical across batch sizes.
+ * The host arrays are consumed before the call returns, so the call can be
+ * captured into a CUDA graph and replayed.  Validates every matrix before
+ * launching any.
  */
 q4_status q4_decode_step(const q4_matrix* mats, int n_mats,
                          const uint16_t* const* X, float* const* Y, int B,
-                         void* ws, size_t ws_bytes, void* stream);
+                         void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/* Workspace q4_decode_step needs for matrices of shapes (N[i], K[i]), batch B and
+ * `flags` on the current device (0 for invalid input). */
+size_t q4_decode_step_workspace_bytes(const int64_t* N, const int64_t* K, int n_mats, int B,
+                                      unsigned flags);
+
+/*
+ * The two phases of q4_decode_step for an independent list whose matrices all
+ * carry the tiled copy.
+ *
+ * q4_step_workspace_bytes -- bytes of device workspace both phases need for
+ * matrices of input widths K[i] at batch B: the prepared activations, about
+ * (K/128) * (256 * BT + 32) bytes per matrix, BT = B rounded up to 1, 2, 4 or 8.
+ * 0 for invalid input.
+ *
+ * q4_step_prepare -- stage each X[i] (device bf16 [B, K_i], 16-byte aligned)
+ * once into ws: in mma B-fragment order, times a power of two per batch column
+ * (so that the products of codes and activations are normal fp32 numbers), with
+ * the sum of every 128-column group and the per-column factors that undo the
+ * scaling.  One launch per 128 matrices, one CTA per matrix.
+ *
+ * q4_step_stream -- Y[i] = mats[i] X[i] (device fp32 [B, N_i]) from the
+ * activations that the last q4_step_prepare on this ws staged for the same
+ * list (same order, shapes and B).  One persistent launch per 128 matrices,
+ * one CTA per SM: CTA c owns one block of 16-row tiles of every matrix; its
+ * warps take whole tiles from a shared counter, matrix after matrix, with no
+ * block-wide barrier, and add all groups of a row in order.  Reading ws waits
+ * for the previous kernel in the stream (programmatic dependent launch), so
+ * the two phases may be enqueued back to back and captured in one graph.
+ *
+ * Both: Q4_ERR_INVALID_ARG for null pointers, B outside 1..8 or a matrix
+ * without the tiled copy, Q4_ERR_WORKSPACE if ws_bytes is too small,
+ * Q4_ERR_MISALIGNED / Q4_ERR_UNSUPPORTED_SHAPE as for q4_gemv.
+ */
+size_t q4_step_workspace_bytes(const int64_t* K, int n_mats, int B);
+q4_status q4_step_prepare(const q4_matrix* mats, int n_mats, const uint16_t* const* X, int B,
+                          void* ws, size_t ws_bytes, void* stream);
+q4_status q4_step_stream(const q4_matrix* mats, int n_mats, float* const* Y, int B,
+                         const void* ws, size_t ws_bytes, void* stream);
 
 /*
  * q4_argmax_f32 -- per batch row of logits Y [B, N] (device fp32), the index
@@ -161,6 +246,15 @@ q4_status q4_decode_step(const q4_matrix* mats, int n_mats,
  * Q4_ERR_INVALID_ARG for null pointers, B outside 1..8 or N outside 1..2^31-1.
  */
 q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream);
+
+/*
+ * q4_device_status -- wait for `stream`, then read and clear the device error
+ * word.  Every wait inside the kernels is bounded; one that gives up sets the
+ * word and the kernel carries on to its end (its outputs are then invalid).
+ * Returns Q4_ERR_TIMEOUT if a wait gave up since the last call, Q4_OK if not,
+ * Q4_ERR_CUDA if the stream reports an error.
+ */
+q4_status q4_device_status(void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* q4_status_string(q4_status s);

@@ -17,14 +17,15 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from ._lib import (Q4_OK, Q4Error, check, c_vp, header_functions, lib, q4_matrix,  # noqa: F401
-                   q4_plan_info)
+from ._lib import (Q4_OK, Q4_STEP_INDEPENDENT, Q4Error, check, c_i64, c_vp, header_functions,  # noqa: F401
+                   lib, q4_matrix, q4_plan_info)
 
 GROUP = 128
 MAX_B = 8
 
 __all__ = ["GROUP", "MAX_B", "Q4Error", "QuantizedMatrix", "Workspace", "pack_host", "plan",
-           "workspace_bytes", "gemv", "gemm_skinny", "decode_step", "argmax", "DecodeStepGraph",
+           "workspace_bytes", "decode_step_workspace_bytes", "tiled_bytes", "gemv", "gemm_skinny", "decode_step",
+           "argmax", "device_status", "DecodeStepGraph", "step_workspace_bytes", "step_prepare", "step_stream",
            "header_functions", "lib"]
 
 
@@ -65,30 +66,63 @@ def workspace_bytes(N: int, K: int, B: int = 1) -> int:
     return int(lib.q4_workspace_bytes(N, K, B))
 
 
+def decode_step_workspace_bytes(shapes, B: int, independent: bool = True) -> int:
+    n = len(shapes)
+    Ns = (c_i64 * n)(*[int(N) for N, _ in shapes])
+    Ks = (c_i64 * n)(*[int(K) for _, K in shapes])
+    return int(lib.q4_decode_step_workspace_bytes(Ns, Ks, n, B, Q4_STEP_INDEPENDENT if independent else 0))
+
+
+def device_status(stream=None) -> None:
+    """Wait for the stream and raise Q4Error(Q4_ERR_TIMEOUT) if a bounded device-side wait gave up."""
+    check(lib.q4_device_status(_stream_ptr(stream)), "q4_device_status")
+
+
 # ---------------------------------------------------------------------------- device data
+def tiled_bytes(N: int, K: int) -> int:
+    return int(lib.q4_tiled_bytes(N, K))
+
+
 @dataclass
 class QuantizedMatrix:
-    """One int4 matrix resident on the GPU in the canonical layout."""
-    codes: torch.Tensor   # uint8 [N, K/2]
-    scales: torch.Tensor  # float16 [N, K/128] (the fp16 bit patterns)
-    mins: torch.Tensor    # float16 [N, K/128]
+    """One int4 matrix resident on the GPU: the canonical layout and/or its tiled copy."""
+    codes: torch.Tensor | None   # uint8 [N, K/2]
+    scales: torch.Tensor | None  # float16 [N, K/128] (the fp16 bit patterns)
+    mins: torch.Tensor | None    # float16 [N, K/128]
     N: int
     K: int
+    tiled: torch.Tensor | None = None  # uint8 [tiled_bytes(N, K)]
 
     @classmethod
-    def from_packed(cls, codes: np.ndarray, scales: np.ndarray, mins: np.ndarray, device="cuda"):
+    def from_packed(cls, codes: np.ndarray, scales: np.ndarray, mins: np.ndarray, device="cuda",
+                    tiled: bool = True, keep_canonical: bool = True, stream=None):
         N, H = codes.shape
         c = torch.from_numpy(np.ascontiguousarray(codes)).to(device)
         s = torch.from_numpy(np.ascontiguousarray(scales).view(np.float16)).to(device)
         m = torch.from_numpy(np.ascontiguousarray(mins).view(np.float16)).to(device)
-        return cls(c, s, m, N, 2 * H)
+        W = cls(c, s, m, N, 2 * H)
+        if tiled:
+            W.build_tiled(stream)
+            if not keep_canonical:
+                torch.cuda.current_stream(c.device).synchronize()
+                W.codes = W.scales = W.mins = None
+        return W
 
     @classmethod
-    def from_float(cls, w: np.ndarray, device="cuda", n_threads: int = 0):
-        return cls.from_packed(*pack_host(w, n_threads), device=device)
+    def from_float(cls, w: np.ndarray, device="cuda", n_threads: int = 0, tiled: bool = True):
+        return cls.from_packed(*pack_host(w, n_threads), device=device, tiled=tiled)
+
+    def build_tiled(self, stream=None):
+        """Build the tiled copy (q4_tile) from the canonical arrays."""
+        nb = tiled_bytes(self.N, self.K)
+        self.tiled = torch.empty(nb, dtype=torch.uint8, device=self.codes.device)
+        m = self.c_struct()
+        check(lib.q4_tile(ctypes.byref(m), _ptr(self.tiled), nb, _stream_ptr(stream)), "q4_tile")
+        return self
 
     def c_struct(self) -> q4_matrix:
-        return q4_matrix(_ptr(self.codes), _ptr(self.scales), _ptr(self.mins), self.N, self.K)
+        p = lambda t: _ptr(t) if t is not None else None
+        return q4_matrix(p(self.codes), p(self.scales), p(self.mins), self.N, self.K, p(self.tiled))
 
 
 class Workspace:
@@ -99,9 +133,8 @@ class Workspace:
         self.buf = torch.zeros(max(self.nbytes, 16), dtype=torch.uint8, device=device) if self.nbytes else None
 
     @classmethod
-    def for_shapes(cls, shapes, B: int = MAX_B, device="cuda"):
-        need = max([workspace_bytes(N, K, B) for N, K in shapes] + [0])
-        return cls(need, device)
+    def for_shapes(cls, shapes, B: int = MAX_B, device="cuda", independent: bool = True):
+        return cls(decode_step_workspace_bytes(shapes, B, independent), device)
 
     def ptr(self) -> int:
         return _ptr(self.buf) if self.buf is not None else 0
@@ -150,15 +183,48 @@ def gemv(W: QuantizedMatrix, x: torch.Tensor, y: torch.Tensor | None = None,
     return y
 
 
-def decode_step(mats, Xs, Ys, workspace: Workspace | None = None, stream=None) -> None:
-    """Enqueue one decode step: Ys[i] = mats[i] Xs[i] for every matrix, in list order."""
+def decode_step(mats, Xs, Ys, workspace: Workspace | None = None, stream=None, independent: bool = True) -> None:
+    """Enqueue one decode step: Ys[i] = mats[i] Xs[i] for every matrix, in list order.
+
+    independent=True: one persistent launch for the whole list (no Xs[j] may overlap any Ys[i]);
+    False: one launch per matrix, so Ys[i] may feed Xs[j] for j > i."""
     n = len(mats)
     B = Xs[0].shape[0] if Xs[0].dim() == 2 else 1
+    if workspace is None:
+        need = decode_step_workspace_bytes([(m.N, m.K) for m in mats], B, independent)
+        if need:
+            workspace = Workspace(need, Xs[0].device)
     arr = (q4_matrix * n)(*[m.c_struct() for m in mats])
     xp = (c_vp * n)(*[_ptr(_as_bf16(x)) for x in Xs])
     yp = (c_vp * n)(*[_ptr(y) for y in Ys])
     ws_p, ws_n = _ws_args(workspace)
-    check(lib.q4_decode_step(arr, n, xp, yp, B, ws_p, ws_n, _stream_ptr(stream)), "q4_decode_step")
+    flags = Q4_STEP_INDEPENDENT if independent else 0
+    check(lib.q4_decode_step(arr, n, xp, yp, B, ws_p, ws_n, flags, _stream_ptr(stream)), "q4_decode_step")
+
+
+def step_workspace_bytes(Ks, B: int) -> int:
+    n = len(Ks)
+    arr = (c_i64 * n)(*[int(K) for K in Ks])
+    return int(lib.q4_step_workspace_bytes(arr, n, B))
+
+
+def step_prepare(mats, Xs, workspace: Workspace, stream=None) -> None:
+    """Phase 1 of an independent decode step: stage every activation once into the workspace."""
+    n = len(mats)
+    B = Xs[0].shape[0] if Xs[0].dim() == 2 else 1
+    arr = (q4_matrix * n)(*[m.c_struct() for m in mats])
+    xp = (c_vp * n)(*[_ptr(_as_bf16(x)) for x in Xs])
+    check(lib.q4_step_prepare(arr, n, xp, B, workspace.ptr(), workspace.nbytes, _stream_ptr(stream)),
+          "q4_step_prepare")
+
+
+def step_stream(mats, Ys, B: int, workspace: Workspace, stream=None) -> None:
+    """Phase 2: Ys[i] = mats[i] x_i from the activations the last step_prepare staged."""
+    n = len(mats)
+    arr = (q4_matrix * n)(*[m.c_struct() for m in mats])
+    yp = (c_vp * n)(*[_ptr(y) for y in Ys])
+    check(lib.q4_step_stream(arr, n, yp, B, workspace.ptr(), workspace.nbytes, _stream_ptr(stream)),
+          "q4_step_stream")
 
 
 def argmax(Y: torch.Tensor, idx: torch.Tensor | None = None, stream=None) -> torch.Tensor:
@@ -181,15 +247,16 @@ class DecodeStepGraph:
     """
 
     def __init__(self, mats, B: int, X=None, Y=None, workspace: Workspace | None = None, device="cuda",
-                 with_argmax_of: int | None = None):
+                 with_argmax_of: int | None = None, independent: bool = True):
         self.mats = list(mats)
         self.B = B
+        self.independent = independent
         self.X = X if X is not None else [torch.zeros((B, m.K), dtype=torch.bfloat16, device=device)
                                            for m in self.mats]
         self.Y = Y if Y is not None else [torch.empty((B, m.N), dtype=torch.float32, device=device)
                                            for m in self.mats]
         self.ws = workspace if workspace is not None else \
-            Workspace.for_shapes([(m.N, m.K) for m in self.mats], B, device)
+            Workspace.for_shapes([(m.N, m.K) for m in self.mats], B, device, independent)
         self.idx = torch.zeros((B,), dtype=torch.int32, device=device) if with_argmax_of is not None else None
         self.argmax_of = with_argmax_of
         self.graph = torch.cuda.CUDAGraph()
@@ -203,7 +270,7 @@ class DecodeStepGraph:
         torch.cuda.current_stream().wait_stream(side)
 
     def _enqueue(self, stream):
-        decode_step(self.mats, self.X, self.Y, self.ws, stream=stream)
+        decode_step(self.mats, self.X, self.Y, self.ws, stream=stream, independent=self.independent)
         if self.argmax_of is not None:
             argmax(self.Y[self.argmax_of], self.idx, stream=stream)
 

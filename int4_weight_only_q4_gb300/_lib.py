@@ -24,7 +24,7 @@ c_vp = ctypes.c_void_p
 
 
 class q4_matrix(ctypes.Structure):
-    _fields_ = [("codes", c_vp), ("scales", c_vp), ("mins", c_vp), ("N", c_i64), ("K", c_i64)]
+    _fields_ = [("codes", c_vp), ("scales", c_vp), ("mins", c_vp), ("N", c_i64), ("K", c_i64), ("tiled", c_vp)]
 
 
 class q4_plan_info(ctypes.Structure):
@@ -42,9 +42,14 @@ Q4_ERR_MISALIGNED = 3
 Q4_ERR_WORKSPACE = 4
 Q4_ERR_CUDA = 5
 Q4_ERR_TIMEOUT = 6
+Q4_STEP_INDEPENDENT = 1
 
 lib.q4_pack_host.argtypes = [c_vp, c_i64, c_i64, c_vp, c_vp, c_vp, ctypes.c_int]
 lib.q4_pack_host.restype = ctypes.c_int
+lib.q4_tiled_bytes.argtypes = [c_i64, c_i64]
+lib.q4_tiled_bytes.restype = ctypes.c_size_t
+lib.q4_tile.argtypes = [ctypes.POINTER(q4_matrix), c_vp, ctypes.c_size_t, c_vp]
+lib.q4_tile.restype = ctypes.c_int
 lib.q4_workspace_bytes.argtypes = [c_i64, c_i64, ctypes.c_int]
 lib.q4_workspace_bytes.restype = ctypes.c_size_t
 lib.q4_plan.argtypes = [c_i64, c_i64, ctypes.POINTER(q4_plan_info)]
@@ -54,8 +59,21 @@ lib.q4_gemv.restype = ctypes.c_int
 lib.q4_gemm_skinny.argtypes = [ctypes.POINTER(q4_matrix), c_vp, ctypes.c_int, c_vp, c_vp, ctypes.c_size_t, c_vp]
 lib.q4_gemm_skinny.restype = ctypes.c_int
 lib.q4_decode_step.argtypes = [ctypes.POINTER(q4_matrix), ctypes.c_int, ctypes.POINTER(c_vp),
-                               ctypes.POINTER(c_vp), ctypes.c_int, c_vp, ctypes.c_size_t, c_vp]
+                               ctypes.POINTER(c_vp), ctypes.c_int, c_vp, ctypes.c_size_t, ctypes.c_uint, c_vp]
 lib.q4_decode_step.restype = ctypes.c_int
+lib.q4_decode_step_workspace_bytes.argtypes = [ctypes.POINTER(c_i64), ctypes.POINTER(c_i64), ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_uint]
+lib.q4_decode_step_workspace_bytes.restype = ctypes.c_size_t
+lib.q4_step_workspace_bytes.argtypes = [ctypes.POINTER(c_i64), ctypes.c_int, ctypes.c_int]
+lib.q4_step_workspace_bytes.restype = ctypes.c_size_t
+lib.q4_step_prepare.argtypes = [ctypes.POINTER(q4_matrix), ctypes.c_int, ctypes.POINTER(c_vp), ctypes.c_int, c_vp,
+                                ctypes.c_size_t, c_vp]
+lib.q4_step_prepare.restype = ctypes.c_int
+lib.q4_step_stream.argtypes = [ctypes.POINTER(q4_matrix), ctypes.c_int, ctypes.POINTER(c_vp), ctypes.c_int, c_vp,
+                               ctypes.c_size_t, c_vp]
+lib.q4_step_stream.restype = ctypes.c_int
+lib.q4_device_status.argtypes = [c_vp]
+lib.q4_device_status.restype = ctypes.c_int
 lib.q4_argmax_f32.argtypes = [c_vp, ctypes.c_int, c_i64, c_vp, c_vp]
 lib.q4_argmax_f32.restype = ctypes.c_int
 lib.q4_status_string.argtypes = [ctypes.c_int]

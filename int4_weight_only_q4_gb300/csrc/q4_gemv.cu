@@ -2,27 +2,57 @@
 //
 // What is computed (rumik-oss-1 int4 engine page, rtts.neoandmatrix.me,
 // "Step 3" and "Step 7"): Y[b, n] = sum_k (code[n,k] * scale[n,g] + min[n,g]) * X[b,k],
-// g = k / 128, fp32 accumulation.  Every group is evaluated in the folded form
-//     scale * (sum_k (128 + code) x_k)  +  (min - 128 * scale) * (sum_k x_k)
-// so that a code becomes a bf16 operand with one LOP3 (128 + code has the bf16
-// bit pattern 0x4300 | code; the same exponent-field trick the page's CUDA
-// kernel uses with fp16, here with bf16 so it pairs with bf16 activations).
+// g = k / 128, fp32 accumulation.  Every group is evaluated as
+//     scale * (sum_k code_k x_k)  +  min * (sum_k x_k).
+// The page's CUDA kernel turns a code into a float without a conversion by
+// placing it in the mantissa of an fp16 with a fixed exponent (1024 + code).
+// Here the codes become bf16 operands with a single AND per two codes and no
+// offset at all: a bf16 whose exponent field is 0 or 1 and whose low 8 bits
+// hold m has the value m * 2^-133 exactly, so (w & 0x000F000F) is two codes
+// and (w & 0x00F000F0) two codes times 16.  The activations are staged times
+// a per-column power of two (and 1/16 for the high nibbles) that keeps every
+// product a normal fp32 number, and the group sum is multiplied back.  No
+// offset means the accumulator carries only the result (an offset of 128
+// would make it carry 128 * sum(x) and lose ~4 bits).
 //
-// Work split (depends on N, K and the SM count only -- never on B):
-//   grid = row_blocks x k_splits CTAs, one per SM.  CTA (rb, ks) owns rows
-//   [N*rb/RB, N*(rb+1)/RB) and groups [G*ks/KS, G*(ks+1)/KS).  Its rows form
-//   16-row tiles; the (tile, group) units are dealt to the warps in equal
-//   contiguous ranges; a warp's partial sums per tile go to shared memory and
-//   are added in warp order.  With k_splits > 1 the CTA partials go to the
-//   workspace and the last CTA of the row block (arrival ticket) adds them in
-//   k-split order.  Every addition order is therefore fixed by (N, K, SMs),
-//   which makes each batch column bit-identical to the batch-1 result (the
-//   pure-C TTS engine page, wpnews.pro: match the accumulation order).
+// The dot products of a 16-row tile and one group run on the tensor cores:
+// eight mma.m16n8k16 (16 rows x 8 batch columns x 16 k), bf16 in, fp32
+// accumulators; batch columns b >= B are zero.  Because the tensor core
+// computes each output column from its own column of the B operand, column b
+// is the same whatever the other columns hold.
 //
-// Per unit a lane streams 16 bytes of codes of row q and of row q+8 of its
-// tile (q = lane/4) with 128-bit non-allocating loads, DEPTH units ahead.
-// Activations are staged once per CTA in shared memory in the order of the
-// mma B fragment, with the per-group sums of x.
+// Weight layouts.  The canonical layout L0 (include/q4.h) is what the export
+// job writes.  For streaming, each matrix also gets a tiled copy L1 built once
+// on the device (q4_tile): for every 16-row tile j and 128-column group g one
+// contiguous 1,088-byte record
+//     [  0, 512)  lane l's 16 code bytes of row 16j + l/4, columns 32(l%4)..+31
+//     [512,1024)  the same for row 16j + l/4 + 8
+//     [1024,1088) for q = 0..7: scale|min<<16 of row 16j+q, then of row 16j+q+8
+// records ordered tile-major (j, then g).  A warp reads a record with two
+// 512-byte loads and one 64-byte load, all contiguous; a CTA's rows are one
+// contiguous byte range; a run of groups of one tile is one bulk copy.
+//
+// Work split (depends on N, K and the SM count only -- never on B): CTA
+// (rb, ks) owns a block of rows (whole 16-row tiles for L1) and groups
+// [G*ks/KS, G*(ks+1)/KS).  Inside a CTA the (tile, group) units are dealt to
+// the warps in contiguous ranges (direct kernel) or streamed in chunks of 8
+// groups (stream kernel); partial sums are added in a fixed order (warp order
+// or chunk order), and with KS > 1 the CTA results go to the workspace and
+// the last CTA of the row block (arrival ticket) adds them in k-split order.
+// Every addition order is therefore fixed by (N, K, SMs), which makes each
+// batch column bit-identical to the batch-1 result (the pure-C TTS engine
+// page, wpnews.pro: match the accumulation order).
+//
+// Kernels.  "direct": one CTA per SM, persistent over a list of matrices;
+// every lane loads its codes straight into registers DEPTH units ahead, and
+// the first units of the next matrix are in flight while the current one is
+// being finished.  "stream": a producer warp streams chunks of L1 records with
+// 1-D bulk copies (cp.async.bulk) into a shared-memory ring guarded by
+// mbarriers; consumer warp w owns stages w, w+W, ..., w+(D-1)W and takes every
+// W-th chunk, so it waits for a round of a stage only after it has released
+// the previous round itself and the mbarrier phase parity cannot alias.
+// Both stage the activations per matrix in shared memory in B-fragment order
+// with the per-group sums of x.
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -40,18 +70,15 @@ constexpr int64_t kMaxK = 65536;
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 220 * 1024;  // dynamic; leaves room for static smem under the 227 KB cap
 
-struct GemvArgs {
-    const uint8_t* codes;
-    const uint16_t* scales;
-    const uint16_t* mins;
-    const uint16_t* x;
-    float* y;
-    float* ws_part;          // [k_splits][B][N] when k_splits > 1
-    unsigned int* ws_cnt;    // [row_blocks]
-    int N, K, B;
-    int row_blocks, k_splits, smax;
-    int l2_prefetch;         // bytes of this CTA's codes to bulk-prefetch into L2 up front
-};
+constexpr int kRecBytes = 1088;                 // one L1 record: 16 rows x 128 columns + scale/min
+constexpr int kKC = 8;                          // groups (records) per streamed chunk
+constexpr int kStageBytes = kKC * kRecBytes;    // one stream-ring stage
+constexpr int kMaxMats = 128;                   // matrices per stream launch (kernel parameter table)
+constexpr int kHdrBytes = 512;                  // ring header: up to 2 x 24 mbarriers + the k-split flag
+constexpr unsigned kDefaultWaitLimit = 1u << 22;
+
+// Device-side error word: bit 0 = a bounded barrier wait gave up.
+__device__ unsigned int g_q4_device_error;
 
 // ------------------------------------------------------------------ device helpers
 __device__ __forceinline__ uint4 ld_stream_u4(const uint8_t* p) {
@@ -62,17 +89,16 @@ __device__ __forceinline__ uint4 ld_stream_u4(const uint8_t* p) {
     return r;
 }
 
+__device__ __forceinline__ uint2 ld_stream_u2(const uint8_t* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t ld_nc_u16(const uint16_t* p) {
     unsigned short v;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
-}
-
-// bf16x2 {128 + (v & 15), 128 + ((v >> 16) & 15)}: (v & 0x000F000F) | 0x43004300
-__device__ __forceinline__ uint32_t bf16x2_of_nibbles(uint32_t v) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x43004300u));
-    return r;
 }
 
 __device__ __forceinline__ void mma_bf16_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -87,23 +113,409 @@ __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_fl
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 __device__ __forceinline__ float half_bits_to_f32(uint32_t h) {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
 }
 
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void allow_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Ask L2 to fetch [p, p + bytes) from DRAM (bytes: multiple of 16, p: 16-byte aligned).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Wait for the phase with the given parity to complete, at most `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    const uint32_t a = smem_addr(bar);
+    for (uint32_t it = 0; it < limit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void report_timeout() { atomicOr(&g_q4_device_error, 1u); }
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes: multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_addr(p)));
+    return r;
+}
+
+__device__ __forceinline__ uint2 lds64(const unsigned char* p) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(smem_addr(p)));
+    return r;
+}
+
+template <int NTHREADS>
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
+}
+
+// ------------------------------------------------------------------ one 16-row x 128-column group
+// Codes as bf16 operands without arithmetic: a bf16 whose exponent field is 0 or 1 and whose
+// low 8 bits hold m is exactly m * 2^-133 (the subnormals continue into the first normal
+// binade with the same spacing).  So w & 0x000F000F is the bf16 pair {c0, c4} * 2^-133 and
+// w & 0x00F000F0 is {c1, c5} * 16 * 2^-133 -- one LOP3 per two codes, no offset to remove.
+// The activations are staged multiplied by 2^a (paired with low nibbles) or 2^(a-4) (paired
+// with high nibbles), a chosen per batch column so the products stay normal fp32 numbers, and
+// the epilogue multiplies the group sum by 2^(133-a).  Every step is exact except the fp32
+// additions.
+__device__ __forceinline__ uint32_t lo_nibbles(uint32_t v) { return v & 0x000F000Fu; }
+__device__ __forceinline__ uint32_t hi_nibbles(uint32_t v) { return v & 0x00F000F0u; }
+
+// Fragment-order x: entry (group gl, word i, half p, lane 4n+t), BT entries per lane quad.
+template <int BT>
+__device__ __forceinline__ size_t xfrag_index(int gl, int i, int p) {
+    return (static_cast<size_t>(gl) * 8 + i * 2 + p) * (4 * BT);
+}
+
+// qa/qb: this lane's 32 codes (16 bytes) of tile rows q and q+8, columns 32t..32t+31 of the group.
+// xg: the group's staged activations.  c: rows (q, q, q+8, q+8) x batch columns (2t, 2t+1, 2t,
+// 2t+1) of sum_k code * x * 2^(a-133).
+// Loads of data the previous kernel in the stream wrote (activations, their prepared copy,
+// logits): ordinary coherent loads, in volatile asm so that they stay after the
+// griddepcontrol.wait that makes that data visible.  (A non-coherent ld.global.nc is only
+// valid for data that is read-only for the whole life of the kernel, and the compiler may move
+// it above the wait.)
+__device__ __forceinline__ uint2 ld_dep_u2(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p) : "memory");
+    return r;
+}
+__device__ __forceinline__ float ld_dep_f32(const float* p) {
+    float r;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(r) : "l"(p) : "memory");
+    return r;
+}
+
+template <bool GLOBAL>
+__device__ __forceinline__ uint2 ld_x(const uint2* p) {
+    if constexpr (GLOBAL) return ld_dep_u2(p);
+    return *p;
+}
+
+template <bool MMA, int BT, bool XG = false>
+__device__ __forceinline__ void group_dot(const uint4& qa, const uint4& qb, const uint2* xg, int lane, int B,
+                                          float (&c)[4]) {
+    const int t = lane & 3, q = lane >> 2;
+    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+    const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+    c[0] = c[1] = c[2] = c[3] = 0.f;
+    if constexpr (MMA) {
+        const bool xon = q < B;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // word i holds columns 8i..8i+7 of the lane's 32: pairs (0,4) (1,5) | (2,6) (3,7)
+            const uint32_t wa8 = wa[i] >> 8, wb8 = wb[i] >> 8;
+            uint2 x0 = make_uint2(0, 0), x1 = make_uint2(0, 0);
+            if (xon) {
+                x0 = ld_x<XG>(xg + xfrag_index<BT>(0, i, 0) + lane);
+                x1 = ld_x<XG>(xg + xfrag_index<BT>(0, i, 1) + lane);
+            }
+            mma_bf16_m16n8k16(c, lo_nibbles(wa[i]), lo_nibbles(wb[i]), hi_nibbles(wa[i]), hi_nibbles(wb[i]), x0.x,
+                              x0.y);
+            mma_bf16_m16n8k16(c, lo_nibbles(wa8), lo_nibbles(wb8), hi_nibbles(wa8), hi_nibbles(wb8), x1.x, x1.y);
+        }
+    } else {
+        float pa[BT], pb[BT];
+#pragma unroll
+        for (int n = 0; n < BT; ++n) { pa[n] = 0.f; pb[n] = 0.f; }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const uint32_t va = wa[i] >> (8 * p), vb = wb[i] >> (8 * p);
+                const uint32_t A0 = lo_nibbles(va), A1 = hi_nibbles(va);
+                const uint32_t B0 = lo_nibbles(vb), B1 = hi_nibbles(vb);
+                const float a00 = bf16lo_to_f32(A0), a01 = bf16hi_to_f32(A0);
+                const float a10 = bf16lo_to_f32(A1), a11 = bf16hi_to_f32(A1);
+                const float b00 = bf16lo_to_f32(B0), b01 = bf16hi_to_f32(B0);
+                const float b10 = bf16lo_to_f32(B1), b11 = bf16hi_to_f32(B1);
+#pragma unroll
+                for (int n = 0; n < BT; ++n) {
+                    uint2 xv = make_uint2(0, 0);
+                    if (n < B) xv = ld_x<XG>(xg + xfrag_index<BT>(0, i, p) + n * 4 + t);
+                    const float x00 = bf16lo_to_f32(xv.x), x01 = bf16hi_to_f32(xv.x);
+                    const float x10 = bf16lo_to_f32(xv.y), x11 = bf16hi_to_f32(xv.y);
+                    pa[n] = fmaf(a00, x00, pa[n]);
+                    pa[n] = fmaf(a01, x01, pa[n]);
+                    pa[n] = fmaf(a10, x10, pa[n]);
+                    pa[n] = fmaf(a11, x11, pa[n]);
+                    pb[n] = fmaf(b00, x00, pb[n]);
+                    pb[n] = fmaf(b01, x01, pb[n]);
+                    pb[n] = fmaf(b10, x10, pb[n]);
+                    pb[n] = fmaf(b11, x11, pb[n]);
+                }
+            }
+        }
+        // add the quad's four 32-column pieces; every lane of the quad gets the same value
+#pragma unroll
+        for (int n = 0; n < BT; ++n) {
+            pa[n] += __shfl_xor_sync(0xffffffffu, pa[n], 1);
+            pa[n] += __shfl_xor_sync(0xffffffffu, pa[n], 2);
+            pb[n] += __shfl_xor_sync(0xffffffffu, pb[n], 1);
+            pb[n] += __shfl_xor_sync(0xffffffffu, pb[n], 2);
+        }
+#pragma unroll
+        for (int n = 0; n < BT; ++n) {
+            if (n == 2 * t) { c[0] = pa[n]; c[2] = pb[n]; }
+            if (n == 2 * t + 1) { c[1] = pa[n]; c[3] = pb[n]; }
+        }
+    }
+}
+
+// acc += scale * (c * f) + min * S for rows q (scale/min packed in sa_ma) and q+8 (sb_mb);
+// f = 2^(133-a) of batch columns 2t, 2t+1 undoes the staging scale.
+template <bool XG = false>
+__device__ __forceinline__ void group_epilogue(float (&acc)[4], const float (&c)[4], uint32_t sa_ma,
+                                               uint32_t sb_mb, const float* S2, float f0, float f1) {
+    float2 S;
+    if constexpr (XG) {
+        const uint2 v = ld_dep_u2(S2);
+        S = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+    } else {
+        S = *reinterpret_cast<const float2*>(S2);
+    }
+    const float sa = half_bits_to_f32(sa_ma), ma = half_bits_to_f32(sa_ma >> 16);
+    const float sb = half_bits_to_f32(sb_mb), mb = half_bits_to_f32(sb_mb >> 16);
+    acc[0] = fmaf(sa, c[0] * f0, acc[0]);
+    acc[0] = fmaf(ma, S.x, acc[0]);
+    acc[1] = fmaf(sa, c[1] * f1, acc[1]);
+    acc[1] = fmaf(ma, S.y, acc[1]);
+    acc[2] = fmaf(sb, c[2] * f0, acc[2]);
+    acc[2] = fmaf(mb, S.x, acc[2]);
+    acc[3] = fmaf(sb, c[3] * f1, acc[3]);
+    acc[3] = fmaf(mb, S.y, acc[3]);
+}
+
+// bf16 pair times m1 * m2 (powers of two), exact for the supported range (see stage_x).
+__device__ __forceinline__ uint32_t bf16x2_scale(uint32_t v, float m1, float m2) {
+    const float lo = (bf16lo_to_f32(v) * m1) * m2, hi = (bf16hi_to_f32(v) * m1) * m2;
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Stage x[:, 128*g0 .. 128*(g0+Gs)) in B-fragment order, the per-group sums of x and the
+// per-column factors.  Column n gets a_n = 120 - e_n (e_n = exponent of the largest |x| of the
+// column's slice, a_n in [6, 253]): entries pairing with low nibbles hold x * 2^a_n, with high
+// nibbles x * 2^(a_n-4), and fac[n] = 2^(133 - a_n).  Exact for |x| < 2^121.
+// Entry (gl, i, p, lane = 4n + t) (8 bytes) holds x[n][k], k = 128(g0+gl) + 32t + 8i + {2p, 2p+4,
+// 2p+1, 2p+5}; S[gl][n] = sum over the group (fixed order: 8 sequential adds, then a 16-lane xor
+// tree).  Every thread in [0, nthr) calls this; nthr is a multiple of 32.  colmax: 8 words of
+// scratch shared memory.
+template <int BT, typename Sync>
+__device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0, int Gs, uint2* xs, float* ssum,
+                                        float* fac, unsigned* colmax, int tid, int nthr, Sync sync) {
+    const int items = Gs * B * 16;  // (local group, column, chunk t, word i); (t, i) fastest
+    const int iters = (items + nthr - 1) / nthr;
+    if (tid < 8) colmax[tid] = 0u;
+    sync();
+    for (int it = 0; it < iters; ++it) {
+        const int idx = it * nthr + tid;
+        float s = 0.f;
+        const bool on = idx < items;
+        int gl = 0, n = 0;
+        if (on) {
+            const int ti = idx & 15;
+            const int gn = idx >> 4;
+            n = gn % B;
+            gl = gn / B;
+            const int tt = ti >> 2, i = ti & 3;
+            const uint4 v = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(n) * K +
+                                                            static_cast<size_t>(g0 + gl) * 128 + tt * 32 + i * 8);
+            uint32_t mx = 0;
+            const uint32_t h[8] = {v.x << 16, v.x & 0xFFFF0000u, v.y << 16, v.y & 0xFFFF0000u,
+                                   v.z << 16, v.z & 0xFFFF0000u, v.w << 16, v.w & 0xFFFF0000u};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx = max(mx, h[e] & 0x7FFFFFFFu);
+            atomicMax(&colmax[n], mx);
+            s = bf16lo_to_f32(v.x);
+            s += bf16hi_to_f32(v.x);
+            s += bf16lo_to_f32(v.y);
+            s += bf16hi_to_f32(v.y);
+            s += bf16lo_to_f32(v.z);
+            s += bf16hi_to_f32(v.z);
+            s += bf16lo_to_f32(v.w);
+            s += bf16hi_to_f32(v.w);
+        }
+        s += __shfl_xor_sync(0xffffffffu, s, 8);
+        s += __shfl_xor_sync(0xffffffffu, s, 4);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        if (on && (idx & 15) == 0) ssum[gl * 8 + n] = s;
+    }
+    for (int idx = tid; idx < Gs * 8; idx += nthr)
+        if ((idx & 7) >= B) ssum[idx] = 0.f;
+    sync();
+    for (int idx = tid; idx < items; idx += nthr) {
+        const int ti = idx & 15;
+        const int gn = idx >> 4;
+        const int n = gn % B;
+        const int gl = gn / B;
+        const int tt = ti >> 2, i = ti & 3;
+        const int e = static_cast<int>(colmax[n] >> 23) - 127;  // colmax == 0: e = -127
+        int a = 120 - e;
+        a = a < 6 ? 6 : (a > 253 ? 253 : a);
+        const uint4 v = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(n) * K +
+                                                        static_cast<size_t>(g0 + gl) * 128 + tt * 32 + i * 8);
+        // x * 2^a as two exact power-of-two products, so that 2^a itself need not be a float
+        const int a1 = a > 127 ? 127 : a;
+        const float m1 = __int_as_float((a1 + 127) << 23);
+        const float m2 = __int_as_float((a - a1 + 127) << 23);
+        uint2 p0, p1;
+        p0.x = __byte_perm(v.x, v.z, 0x5410);
+        p0.y = __byte_perm(v.x, v.z, 0x7632);
+        p1.x = __byte_perm(v.y, v.w, 0x5410);
+        p1.y = __byte_perm(v.y, v.w, 0x7632);
+        p0.x = bf16x2_scale(p0.x, m1, m2);
+        p1.x = bf16x2_scale(p1.x, m1, m2);
+        p0.y = bf16x2_scale(p0.y, m1, m2 * 0.0625f);
+        p1.y = bf16x2_scale(p1.y, m1, m2 * 0.0625f);
+        const size_t base = xfrag_index<BT>(gl, i, 0) + n * 4 + tt;
+        xs[base] = p0;
+        xs[base + 4 * BT] = p1;
+    }
+    if (tid < 8) {
+        const int e = static_cast<int>(colmax[tid] >> 23) - 127;
+        int a = 120 - e;
+        a = a < 6 ? 6 : (a > 253 ? 253 : a);
+        fac[tid] = __int_as_float((133 - a + 127) << 23);  // 2^(133-a), 2^-120 .. 2^127
+    }
+}
+
+// ================================================================== L1 tiled layout
+// One thread per 16-byte piece of a record: pieces 0..63 are code bytes, 64..67 scale/min.
+__global__ void q4_tile_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                               const uint16_t* __restrict__ mins, int N, int K, uint8_t* __restrict__ tiled,
+                               int64_t pieces) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= pieces) return;
+    const int G = K >> 7;
+    const int64_t rec = idx / 68;
+    const int piece = static_cast<int>(idx - rec * 68);
+    const int j = static_cast<int>(rec / G);
+    const int g = static_cast<int>(rec - static_cast<int64_t>(j) * G);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (piece < 64) {
+        const int h = piece >> 5, l = piece & 31;
+        const int row = 16 * j + (l >> 2) + 8 * h;
+        if (row < N)
+            v = *reinterpret_cast<const uint4*>(codes + static_cast<size_t>(row) * (K >> 1) + g * 64 + (l & 3) * 16);
+    } else {
+        const int pp = piece - 64;  // q = 2pp and 2pp + 1
+        uint32_t w[4] = {0, 0, 0, 0};
+        for (int e = 0; e < 2; ++e) {
+            const int q = 2 * pp + e;
+            for (int h = 0; h < 2; ++h) {
+                const int row = 16 * j + q + 8 * h;
+                if (row < N) {
+                    const size_t o = static_cast<size_t>(row) * G + g;
+                    w[2 * e + h] = static_cast<uint32_t>(scales[o]) | (static_cast<uint32_t>(mins[o]) << 16);
+                }
+            }
+        }
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    *reinterpret_cast<uint4*>(tiled + rec * kRecBytes + piece * 16) = v;
+}
+
+// ================================================================== work lists
+struct MatDesc {
+    const uint8_t* codes;     // L0 (may be null when `tiled` is used)
+    const uint16_t* scales;
+    const uint16_t* mins;
+    const uint8_t* tiled;     // L1 records (may be null for the L0 kernels)
+    const uint16_t* x;
+    float* y;
+    float* ws_part;           // [k_splits][B][N] when k_splits > 1
+    unsigned* ws_cnt;         // [row_blocks][passes]
+    int N, K;
+    int row_blocks, k_splits, tiles_per_pass, passes, smax;
+    int rot;                  // CTA c takes row block (c / k_splits + rot) % row_blocks
+};
+
+struct Params {
+    int n_mats;
+    int B;
+    unsigned wait_limit;
+    int l2_ahead;  // direct kernel on L1: records each warp asks L2 to fetch ahead of its loads (0: off)
+    MatDesc m[kMaxMats];
+};
+
+struct Share {
+    int rb, ks, r0, r1, t0, g0, Gs, T;
+};
+
+// The part of matrix m that CTA `cta` computes; false if it has none.  TILE_GRAIN: row blocks
+// are whole 16-row tiles (L1); otherwise any rows (L0).
+template <bool TILE_GRAIN>
+__device__ __forceinline__ bool cta_share(const MatDesc& m, int cta, Share& s) {
+    if (cta >= m.row_blocks * m.k_splits) return false;
+    const int G = m.K >> 7;
+    const int rbx = cta / m.k_splits;
+    s.ks = cta - rbx * m.k_splits;
+    s.rb = (rbx + m.rot) % m.row_blocks;
+    if (TILE_GRAIN) {
+        const int T_all = (m.N + 15) >> 4;
+        s.t0 = static_cast<int>(static_cast<int64_t>(s.rb) * T_all / m.row_blocks);
+        const int t1 = static_cast<int>(static_cast<int64_t>(s.rb + 1) * T_all / m.row_blocks);
+        s.r0 = 16 * s.t0;
+        s.r1 = min(m.N, 16 * t1);
+    } else {
+        s.r0 = static_cast<int>(static_cast<int64_t>(s.rb) * m.N / m.row_blocks);
+        s.r1 = static_cast<int>(static_cast<int64_t>(s.rb + 1) * m.N / m.row_blocks);
+        s.t0 = 0;
+    }
+    s.g0 = static_cast<int>(static_cast<int64_t>(s.ks) * G / m.k_splits);
+    const int g1 = static_cast<int>(static_cast<int64_t>(s.ks + 1) * G / m.k_splits);
+    s.Gs = g1 - s.g0;
+    s.T = (s.r1 - s.r0 + 15) >> 4;
+    return true;
+}
+
 struct Stage {
-    uint4 qa, qb;                  // 32 codes of row q and of row q+8
-    uint32_t sa, ma, sb, mb;       // fp16 bits of their scale and min
+    uint4 qa, qb;            // 32 codes of row q and of row q+8
+    uint32_t sa_ma, sb_mb;   // fp16 bits: scale | min << 16
 };
 
 // Warp w of WARPS gets units [w*U/WARPS, (w+1)*U/WARPS).
@@ -115,296 +527,519 @@ __device__ __forceinline__ int range_owner(int u, int U, int warps) {
     return static_cast<int>(((static_cast<int64_t>(u) + 1) * warps - 1) / U);
 }
 
-// ------------------------------------------------------------------ the kernel
-// MMA = true: per group, 8 mma.m16n8k16 (16 rows x 8 batch columns x 16 k) with
-// fp32 accumulators.  MMA = false: the same sums on the CUDA cores, BT batch
-// columns, fp32 FMA per code and column; both feed the same epilogue.
-template <int WARPS, int DEPTH, bool MMA, int BT>
-__global__ void __launch_bounds__(WARPS * 32, 1) q4_gemv_kernel(const GemvArgs a) {
-    extern __shared__ __align__(16) unsigned char smem[];
+template <bool TILED>
+__device__ __forceinline__ void load_unit(Stage& s, const MatDesc& m, const Share& sh, int j, int gl, int lane) {
+    const int G = m.K >> 7;
+    if constexpr (TILED) {
+        const uint8_t* rec = m.tiled + (static_cast<size_t>(sh.t0 + j) * G + sh.g0 + gl) * kRecBytes;
+        s.qa = ld_stream_u4(rec + 16 * lane);
+        s.qb = ld_stream_u4(rec + 512 + 16 * lane);
+        const uint2 v = ld_stream_u2(rec + 1024 + 8 * (lane >> 2));
+        s.sa_ma = v.x;
+        s.sb_mb = v.y;
+    } else {
+        const int q = lane >> 2, t = lane & 3;
+        const size_t row_bytes = static_cast<size_t>(m.K) >> 1;
+        const int g = sh.g0 + gl;
+        const int ra = sh.r0 + j * 16 + q;
+        const int rbw = ra + 8;
+        if (ra < sh.r1) {
+            s.qa = ld_stream_u4(m.codes + static_cast<size_t>(ra) * row_bytes + g * 64 + t * 16);
+            s.sa_ma = ld_nc_u16(m.scales + static_cast<size_t>(ra) * G + g) |
+                      (ld_nc_u16(m.mins + static_cast<size_t>(ra) * G + g) << 16);
+        } else {
+            s.qa = make_uint4(0, 0, 0, 0);
+            s.sa_ma = 0;
+        }
+        if (rbw < sh.r1) {
+            s.qb = ld_stream_u4(m.codes + static_cast<size_t>(rbw) * row_bytes + g * 64 + t * 16);
+            s.sb_mb = ld_nc_u16(m.scales + static_cast<size_t>(rbw) * G + g) |
+                      (ld_nc_u16(m.mins + static_cast<size_t>(rbw) * G + g) << 16);
+        } else {
+            s.qb = make_uint4(0, 0, 0, 0);
+            s.sb_mb = 0;
+        }
+    }
+}
+
+// Final per-row sums of a CTA's share: to Y, or through the workspace (k-split, last CTA adds).
+template <int NT, typename Sync>
+__device__ __forceinline__ void finish_rows(const MatDesc& m, const Share& s, int pass, int prow0, int prows, int B,
+                                            int tid, int* flag, Sync sync) {
+    if (m.k_splits <= 1) return;
+    __threadfence();
+    sync();
+    unsigned* cnt = m.ws_cnt + s.rb * m.passes + pass;
+    if (tid == 0) *flag = (atomicAdd(cnt, 1u) == static_cast<unsigned>(m.k_splits - 1));
+    sync();
+    if (*flag) {
+        __threadfence();
+        for (int idx = tid; idx < prows * B; idx += NT) {
+            const int b = idx / prows;
+            const int rr = idx - b * prows;
+            float sum = 0.f;
+            for (int k2 = 0; k2 < m.k_splits; ++k2)
+                sum += __ldcg(m.ws_part + (static_cast<size_t>(k2) * B + b) * m.N + prow0 + rr);
+            m.y[static_cast<size_t>(b) * m.N + prow0 + rr] = sum;
+        }
+        if (tid == 0) *cnt = 0u;  // ready for the next call
+    }
+}
+
+__device__ __forceinline__ void store_row_sum(const MatDesc& m, const Share& s, int b, int row, int B, float v) {
+    if (m.k_splits == 1)
+        m.y[static_cast<size_t>(b) * m.N + row] = v;
+    else
+        m.ws_part[(static_cast<size_t>(s.ks) * B + b) * m.N + row] = v;
+}
+
+// ================================================================== direct kernel
+// Shared memory: x in B-fragment order [Gs*256*B] | x group sums [Gs*8] | warp partials
+// [WARPS][smax][16][B].
+template <int WARPS, int DEPTH, bool TILED, bool MMA, int BT>
+__global__ void __launch_bounds__(WARPS * 32, 1) q4_direct_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int flag;
+    constexpr int NT = WARPS * 32;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int t = lane & 3;    // 16-byte chunk of the 64-byte group row; k-slot quad
-    const int q = lane >> 2;   // tile row (and row q + 8); batch column in the B fragment
-    const int G = a.K >> 7;
-    const int B = a.B;
-    const int rb = blockIdx.x / a.k_splits;
-    const int ks = blockIdx.x - rb * a.k_splits;
-    const int r0 = static_cast<int>(static_cast<int64_t>(rb) * a.N / a.row_blocks);
-    const int r1 = static_cast<int>(static_cast<int64_t>(rb + 1) * a.N / a.row_blocks);
-    const int g0 = static_cast<int>(static_cast<int64_t>(ks) * G / a.k_splits);
-    const int g1 = static_cast<int>(static_cast<int64_t>(ks + 1) * G / a.k_splits);
-    const int Gs = g1 - g0;
-    const int T = (r1 - r0 + 15) >> 4;
-    const int U = T * Gs;
-    const int ub = range_begin(warp, U, WARPS);
-    const int ue = range_begin(warp + 1, U, WARPS);
-    const size_t row_bytes = static_cast<size_t>(a.K) >> 1;
+    const int t = lane & 3;
+    const int q = lane >> 2;
+    const int tid = threadIdx.x;
+    const int B = p.B;
 
-    // shared memory: x in B-fragment order | per-group x sums [Gs][8] | warp partials
-    uint2* xs = reinterpret_cast<uint2*>(smem);
-    float* ssum = reinterpret_cast<float*>(smem + static_cast<size_t>(Gs) * 256 * B);
-    float* part = ssum + Gs * 8;
-
-    if (a.l2_prefetch > 0 && threadIdx.x == 0 && a.k_splits == 1) {
-        // the CTA's codes are one contiguous byte range: rows [r0, r1)
-        const uint8_t* p = a.codes + static_cast<size_t>(r0) * row_bytes;
-        size_t left = static_cast<size_t>(r1 - r0) * row_bytes;
-        if (left > static_cast<size_t>(a.l2_prefetch)) left = static_cast<size_t>(a.l2_prefetch) & ~size_t(15);
-        while (left > 0) {
-            const uint32_t chunk = left > (1u << 20) ? (1u << 20) : static_cast<uint32_t>(left);
-            prefetch_l2_bulk(p, chunk);
-            p += chunk;
-            left -= chunk;
-        }
-    }
-
-    // ---- prologue: start streaming this warp's first DEPTH units (weights are read-only,
-    // so this may run before the previous kernel in the stream has finished)
     Stage st[DEPTH];
-    int lt = 0, lg = 0;  // load cursor: tile, local group
-    if (ub < ue) { lt = ub / Gs; lg = ub - lt * Gs; }
-    auto load_unit = [&](Stage& s) {
-        const int ra = r0 + lt * 16 + q;
-        const int rbw = ra + 8;
-        const int g = g0 + lg;
-        if (ra < r1) {
-            s.qa = ld_stream_u4(a.codes + static_cast<size_t>(ra) * row_bytes + g * 64 + t * 16);
-            s.sa = ld_nc_u16(a.scales + static_cast<size_t>(ra) * G + g);
-            s.ma = ld_nc_u16(a.mins + static_cast<size_t>(ra) * G + g);
-        } else {
-            s.qa = make_uint4(0, 0, 0, 0); s.sa = 0; s.ma = 0;
-        }
-        if (rbw < r1) {
-            s.qb = ld_stream_u4(a.codes + static_cast<size_t>(rbw) * row_bytes + g * 64 + t * 16);
-            s.sb = ld_nc_u16(a.scales + static_cast<size_t>(rbw) * G + g);
-            s.mb = ld_nc_u16(a.mins + static_cast<size_t>(rbw) * G + g);
-        } else {
-            s.qb = make_uint4(0, 0, 0, 0); s.sb = 0; s.mb = 0;
-        }
-        if (++lg == Gs) { lg = 0; ++lt; }
+    int lt = 0, lg = 0;             // load cursor (tile, local group) of the matrix being loaded
+    const uint8_t* lrec = nullptr;  // L1: the record at the cursor
+    auto find_next = [&](int from, Share& s) -> int {
+        for (int i = from; i < p.n_mats; ++i)
+            if (cta_share<TILED>(p.m[i], blockIdx.x, s)) return i;
+        return -1;
     };
+    int lu = 0, lue = 0;            // unit index at the cursor and the end of this warp's range
+    // load the unit at the cursor and advance it (consecutive units are consecutive records
+    // except where a tile ends inside a k-split); with one k-split, also ask L2 for the record
+    // l2_ahead units further on, so that DRAM sees far more requests than registers can hold
+    auto load_next = [&](Stage& sg, const MatDesc& mm, const Share& s) {
+        if constexpr (TILED) {
+            if (p.l2_ahead > 0 && mm.k_splits == 1 && lane == 0 && lu + p.l2_ahead < lue)
+                prefetch_l2_bulk(lrec + static_cast<size_t>(p.l2_ahead) * kRecBytes, kRecBytes);
+            ++lu;
+            sg.qa = ld_stream_u4(lrec + 16 * lane);
+            sg.qb = ld_stream_u4(lrec + 512 + 16 * lane);
+            const uint2 v = ld_stream_u2(lrec + 1024 + 8 * q);
+            sg.sa_ma = v.x;
+            sg.sb_mb = v.y;
+            lrec += kRecBytes;
+            if (++lg == s.Gs) {
+                lg = 0;
+                ++lt;
+                lrec += static_cast<size_t>((mm.K >> 7) - s.Gs) * kRecBytes;
+            }
+        } else {
+            load_unit<false>(sg, mm, s, lt, lg, lane);
+            if (++lg == s.Gs) { lg = 0; ++lt; }
+        }
+    };
+    // issue the first DEPTH loads of this warp's range of matrix i
+    auto prologue = [&](int i, const Share& s, int ub, int ue) {
+        if (ub < ue) {
+            lt = ub / s.Gs;
+            lg = ub - lt * s.Gs;
+            lu = ub;
+            lue = ue;
+            if constexpr (TILED) {
+                lrec = p.m[i].tiled +
+                       (static_cast<size_t>(s.t0 + lt) * (p.m[i].K >> 7) + s.g0 + lg) * kRecBytes;
+                // the records between the first loads and the steady-state prefetch front
+                if (p.l2_ahead > DEPTH && p.m[i].k_splits == 1 && lane == 0) {
+                    const int a = ub + DEPTH, b = min(ue, ub + p.l2_ahead);
+                    if (a < b)
+                        prefetch_l2_bulk(lrec + static_cast<size_t>(DEPTH) * kRecBytes,
+                                         static_cast<uint32_t>((b - a) * kRecBytes));
+                }
+            }
+        }
 #pragma unroll
-    for (int d = 0; d < DEPTH; ++d)
-        if (ub + d < ue) load_unit(st[d]);
+        for (int d = 0; d < DEPTH; ++d)
+            if (ub + d < ue) load_next(st[d], p.m[i], s);
+    };
 
-    grid_dependency_wait();   // x may be the previous kernel's output; ws is shared with it
+    Share cs;
+    int ci = find_next(0, cs);
+    int cU = 0, cub = 0, cue = 0;
+    if (ci >= 0) {
+        cU = cs.T * cs.Gs;
+        cub = range_begin(warp, cU, WARPS);
+        cue = range_begin(warp + 1, cU, WARPS);
+        prologue(ci, cs, cub, cue);  // weights are read-only: may run before the previous kernel ends
+    }
+    grid_dependency_wait();  // x may be the previous kernel's output; y and ws are shared with it
     allow_dependents();
 
-    // ---- stage x in B-fragment order and the per-group sums of x
-    {
-        const int items = Gs * B * 16;  // (local group, column, chunk t, word i); (t, i) fastest
-        const int iters = (items + blockDim.x - 1) / blockDim.x;
-        for (int it = 0; it < iters; ++it) {
-            const int idx = it * blockDim.x + threadIdx.x;
-            float s = 0.f;
-            const bool on = idx < items;
-            int gl = 0, n = 0;
-            if (on) {
-                const int ti = idx & 15;
-                const int gn = idx >> 4;
-                n = gn % B;
-                gl = gn / B;
-                const int tt = ti >> 2, i = ti & 3;
-                const uint4 v = *reinterpret_cast<const uint4*>(
-                    a.x + static_cast<size_t>(n) * a.K + static_cast<size_t>(g0 + gl) * 128 + tt * 32 + i * 8);
-                // v holds x[e0..e7] (two per word); fragment pairs are (e0,e4),(e1,e5) | (e2,e6),(e3,e7)
-                uint2 p0, p1;
-                p0.x = __byte_perm(v.x, v.z, 0x5410);
-                p0.y = __byte_perm(v.x, v.z, 0x7632);
-                p1.x = __byte_perm(v.y, v.w, 0x5410);
-                p1.y = __byte_perm(v.y, v.w, 0x7632);
-                const size_t base = static_cast<size_t>(gl * 4 + i) * 2 * (4 * B) + n * 4 + tt;
-                xs[base] = p0;
-                xs[base + 4 * B] = p1;
-                s = bf16lo_to_f32(v.x);
-                s += bf16hi_to_f32(v.x);
-                s += bf16lo_to_f32(v.y);
-                s += bf16hi_to_f32(v.y);
-                s += bf16lo_to_f32(v.z);
-                s += bf16hi_to_f32(v.z);
-                s += bf16lo_to_f32(v.w);
-                s += bf16hi_to_f32(v.w);
-            }
-            s += __shfl_xor_sync(0xffffffffu, s, 8);
-            s += __shfl_xor_sync(0xffffffffu, s, 4);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            if (on && (idx & 15) == 0) ssum[gl * 8 + n] = s;
-        }
-        for (int idx = threadIdx.x; idx < Gs * 8; idx += blockDim.x)
-            if ((idx & 7) >= B) ssum[idx] = 0.f;
-    }
-    __syncthreads();
+    while (ci >= 0) {
+        const MatDesc& m = p.m[ci];
+        uint2* xs = reinterpret_cast<uint2*>(smem);
+        float* ssum = reinterpret_cast<float*>(smem + static_cast<size_t>(cs.Gs) * 256 * BT);
+        float* fac = ssum + cs.Gs * 8;
+        unsigned* colmax = reinterpret_cast<unsigned*>(fac + 8);
+        float* part = reinterpret_cast<float*>(colmax + 8);
+        stage_x<BT>(m.x, m.K, B, cs.g0, cs.Gs, xs, ssum, fac, colmax, tid, NT, [] { __syncthreads(); });
+        __syncthreads();
+        const float f0 = fac[2 * t], f1 = fac[2 * t + 1];
 
-    // ---- main loop over this warp's units
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // rows (q, q, q+8, q+8) x columns (2t, 2t+1, 2t, 2t+1)
-    int ct = (ub < ue) ? ub / Gs : 0;     // compute cursor
-    int cg = (ub < ue) ? ub - ct * Gs : 0;
-    int seg = 0;
-    const int first_tile = ct;
-    const bool xon = q < B;
-
-    auto flush = [&](int tile) {
-        if (tile - first_tile >= a.smax) return;  // cannot happen with a plan from make_plan
-        float* pp = part + static_cast<size_t>(warp * a.smax + (tile - first_tile)) * 16 * B;
-        const int c0 = 2 * t, c1 = 2 * t + 1;
-        if (c0 < B) { pp[q * B + c0] = acc[0]; pp[(q + 8) * B + c0] = acc[2]; }
-        if (c1 < B) { pp[q * B + c1] = acc[1]; pp[(q + 8) * B + c1] = acc[3]; }
-    };
-
-    auto compute_unit = [&](const Stage& s) {
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t wa[4] = {s.qa.x, s.qa.y, s.qa.z, s.qa.w};
-        const uint32_t wb[4] = {s.qb.x, s.qb.y, s.qb.z, s.qb.w};
-        const uint2* xg = xs + static_cast<size_t>(cg) * 8 * (4 * B);
-        if constexpr (MMA) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        int ct = (cub < cue) ? cub / cs.Gs : 0;
+        int cgl = (cub < cue) ? cub - ct * cs.Gs : 0;
+        const int first_tile = ct;
+        auto flush = [&](int tile) {
+            if (tile - first_tile >= m.smax) return;  // cannot happen with a plan from make_plan
+            float* pp = part + static_cast<size_t>(warp * m.smax + (tile - first_tile)) * 16 * B;
+            const int c0 = 2 * t, c1 = 2 * t + 1;
+            if (c0 < B) { pp[q * B + c0] = acc[0]; pp[(q + 8) * B + c0] = acc[2]; }
+            if (c1 < B) { pp[q * B + c1] = acc[1]; pp[(q + 8) * B + c1] = acc[3]; }
+        };
+        for (int u = cub; u < cue; u += DEPTH) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t a0 = bf16x2_of_nibbles(wa[i]);
-                const uint32_t a1 = bf16x2_of_nibbles(wa[i] >> 4);
-                const uint32_t a2 = bf16x2_of_nibbles(wa[i] >> 8);
-                const uint32_t a3 = bf16x2_of_nibbles(wa[i] >> 12);
-                const uint32_t b0 = bf16x2_of_nibbles(wb[i]);
-                const uint32_t b1 = bf16x2_of_nibbles(wb[i] >> 4);
-                const uint32_t b2 = bf16x2_of_nibbles(wb[i] >> 8);
-                const uint32_t b3 = bf16x2_of_nibbles(wb[i] >> 12);
-                uint2 x0 = make_uint2(0, 0), x1 = make_uint2(0, 0);
-                if (xon) {
-                    x0 = xg[(i * 2 + 0) * (4 * B) + lane];
-                    x1 = xg[(i * 2 + 1) * (4 * B) + lane];
-                }
-                mma_bf16_m16n8k16(c, a0, b0, a1, b1, x0.x, x0.y);
-                mma_bf16_m16n8k16(c, a2, b2, a3, b3, x1.x, x1.y);
-            }
-        } else {
-            float pa[BT], pb[BT];
-#pragma unroll
-            for (int n = 0; n < BT; ++n) { pa[n] = 0.f; pb[n] = 0.f; }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    const uint32_t A0 = bf16x2_of_nibbles(wa[i] >> (8 * p));
-                    const uint32_t A1 = bf16x2_of_nibbles(wa[i] >> (8 * p + 4));
-                    const uint32_t B0 = bf16x2_of_nibbles(wb[i] >> (8 * p));
-                    const uint32_t B1 = bf16x2_of_nibbles(wb[i] >> (8 * p + 4));
-                    const float a00 = bf16lo_to_f32(A0), a01 = bf16hi_to_f32(A0);
-                    const float a10 = bf16lo_to_f32(A1), a11 = bf16hi_to_f32(A1);
-                    const float b00 = bf16lo_to_f32(B0), b01 = bf16hi_to_f32(B0);
-                    const float b10 = bf16lo_to_f32(B1), b11 = bf16hi_to_f32(B1);
-#pragma unroll
-                    for (int n = 0; n < BT; ++n) {
-                        uint2 xv = make_uint2(0, 0);
-                        if (n < B) xv = xg[(i * 2 + p) * (4 * B) + n * 4 + t];
-                        const float x00 = bf16lo_to_f32(xv.x), x01 = bf16hi_to_f32(xv.x);
-                        const float x10 = bf16lo_to_f32(xv.y), x11 = bf16hi_to_f32(xv.y);
-                        pa[n] = fmaf(a00, x00, pa[n]);
-                        pa[n] = fmaf(a01, x01, pa[n]);
-                        pa[n] = fmaf(a10, x10, pa[n]);
-                        pa[n] = fmaf(a11, x11, pa[n]);
-                        pb[n] = fmaf(b00, x00, pb[n]);
-                        pb[n] = fmaf(b01, x01, pb[n]);
-                        pb[n] = fmaf(b10, x10, pb[n]);
-                        pb[n] = fmaf(b11, x11, pb[n]);
+            for (int d = 0; d < DEPTH; ++d) {
+                if (u + d < cue) {
+                    const Stage cur = st[d];
+                    if (u + d + DEPTH < cue) load_next(st[d], m, cs);
+                    float cc[4];
+                    group_dot<MMA, BT>(cur.qa, cur.qb, xs + xfrag_index<BT>(cgl, 0, 0), lane, B, cc);
+                    group_epilogue(acc, cc, cur.sa_ma, cur.sb_mb, ssum + cgl * 8 + 2 * t, f0, f1);
+                    if (++cgl == cs.Gs) {
+                        flush(ct);
+                        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                        cgl = 0;
+                        ++ct;
                     }
                 }
             }
-            // sum over the quad's four 32-column chunks; every lane of the quad gets the same value
-#pragma unroll
-            for (int n = 0; n < BT; ++n) {
-                pa[n] += __shfl_xor_sync(0xffffffffu, pa[n], 1);
-                pa[n] += __shfl_xor_sync(0xffffffffu, pa[n], 2);
-                pb[n] += __shfl_xor_sync(0xffffffffu, pb[n], 1);
-                pb[n] += __shfl_xor_sync(0xffffffffu, pb[n], 2);
-            }
-#pragma unroll
-            for (int n = 0; n < BT; ++n) {
-                if (n == 2 * t) { c[0] = pa[n]; c[2] = pb[n]; }
-                if (n == 2 * t + 1) { c[1] = pa[n]; c[3] = pb[n]; }
-            }
         }
-        const float2 S = *reinterpret_cast<const float2*>(ssum + cg * 8 + 2 * t);
-        const float sa = half_bits_to_f32(s.sa), ma = half_bits_to_f32(s.ma);
-        const float sb = half_bits_to_f32(s.sb), mb = half_bits_to_f32(s.mb);
-        const float ma2 = fmaf(-128.f, sa, ma);
-        const float mb2 = fmaf(-128.f, sb, mb);
-        acc[0] = fmaf(sa, c[0], acc[0]);
-        acc[0] = fmaf(ma2, S.x, acc[0]);
-        acc[1] = fmaf(sa, c[1], acc[1]);
-        acc[1] = fmaf(ma2, S.y, acc[1]);
-        acc[2] = fmaf(sb, c[2], acc[2]);
-        acc[2] = fmaf(mb2, S.x, acc[2]);
-        acc[3] = fmaf(sb, c[3], acc[3]);
-        acc[3] = fmaf(mb2, S.y, acc[3]);
-        if (++cg == Gs) {
-            flush(ct);
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            cg = 0;
-            ++ct;
-        }
-    };
+        if (cub < cue && cgl != 0) flush(ct);
 
-    for (int u = ub; u < ue; u += DEPTH) {
-#pragma unroll
-        for (int d = 0; d < DEPTH; ++d) {
-            if (u + d < ue) {
-                const Stage cur = st[d];
-                if (u + d + DEPTH < ue) load_unit(st[d]);
-                compute_unit(cur);
+        // start streaming the next matrix while this one is being finished
+        Share ns;
+        const int ni = find_next(ci + 1, ns);
+        int nU = 0, nub = 0, nue = 0;
+        if (ni >= 0) {
+            nU = ns.T * ns.Gs;
+            nub = range_begin(warp, nU, WARPS);
+            nue = range_begin(warp + 1, nU, WARPS);
+            prologue(ni, ns, nub, nue);
+        }
+        __syncthreads();
+
+        // add the warp partials of each tile in warp order
+        const int rows = cs.r1 - cs.r0;
+        for (int idx = tid; idx < rows * B; idx += NT) {
+            const int b = idx / rows;
+            const int rr = idx - b * rows;
+            const int j = rr >> 4, rl = rr & 15;
+            const int wf = range_owner(j * cs.Gs, cU, WARPS);
+            const int wl = range_owner(j * cs.Gs + cs.Gs - 1, cU, WARPS);
+            float sum = 0.f;
+            for (int w = wf; w <= wl; ++w) {
+                const int bw = range_begin(w, cU, WARPS);
+                if (bw >= range_begin(w + 1, cU, WARPS)) continue;  // empty range
+                sum += part[(static_cast<size_t>(w * m.smax + (j - bw / cs.Gs)) * 16 + rl) * B + b];
             }
+            store_row_sum(m, cs, b, cs.r0 + rr, B, sum);
         }
+        finish_rows<NT>(m, cs, 0, cs.r0, rows, B, tid, &flag, [] { __syncthreads(); });
+        __syncthreads();  // shared memory is restaged for the next matrix
+        ci = ni;
+        cs = ns;
+        cU = nU;
+        cub = nub;
+        cue = nue;
     }
-    if (ub < ue && cg != 0) flush(ct);  // range ended inside a tile
-    (void)seg;
-    __syncthreads();
-
-    // ---- add the warp partials of each tile in warp order
-    const int rows = r1 - r0;
-    const bool split = a.k_splits > 1;
-    for (int idx = threadIdx.x; idx < rows * B; idx += blockDim.x) {
-        const int b = idx / rows;
-        const int rr = idx - b * rows;
-        const int j = rr >> 4, rl = rr & 15;
-        const int wf = range_owner(j * Gs, U, WARPS);
-        const int wl = range_owner(j * Gs + Gs - 1, U, WARPS);
-        float sum = 0.f;
-        for (int w = wf; w <= wl; ++w) {
-            const int bw = range_begin(w, U, WARPS);
-            if (bw >= range_begin(w + 1, U, WARPS)) continue;  // empty range
-            const int sgi = j - bw / Gs;
-            sum += part[(static_cast<size_t>(w * a.smax + sgi) * 16 + rl) * B + b];
-        }
-        if (!split)
-            a.y[static_cast<size_t>(b) * a.N + r0 + rr] = sum;
-        else
-            a.ws_part[(static_cast<size_t>(ks) * B + b) * a.N + r0 + rr] = sum;
-    }
-    if (!split) return;
-
-    // ---- k-split: the last CTA of this row block adds the partials in k-split order
-    __shared__ int is_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned prev = atomicAdd(a.ws_cnt + rb, 1u);
-        is_last = (prev == static_cast<unsigned>(a.k_splits - 1));
-    }
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    for (int idx = threadIdx.x; idx < rows * B; idx += blockDim.x) {
-        const int b = idx / rows;
-        const int rr = idx - b * rows;
-        float sum = 0.f;
-        for (int k2 = 0; k2 < a.k_splits; ++k2)
-            sum += __ldcg(a.ws_part + (static_cast<size_t>(k2) * B + b) * a.N + r0 + rr);
-        a.y[static_cast<size_t>(b) * a.N + r0 + rr] = sum;
-    }
-    if (threadIdx.x == 0) a.ws_cnt[rb] = 0u;  // ready for the next call
 }
 
-// ------------------------------------------------------------------ argmax
+// ================================================================== stream kernel (L1 only)
+// Shared memory: ring [W*D stages of kKC records] | header (mbarriers, flag) | x in B-fragment
+// order | x group sums | chunk partials [tiles_per_pass * cpt][16][B].
+template <int W, int D, bool MMA, int BT>
+__global__ void __launch_bounds__((W + 1) * 32, 1) q4_stream_kernel(const __grid_constant__ Params p) {
+    constexpr int S = W * D;
+    static_assert(2 * S * 8 + 4 <= kHdrBytes, "ring header too small");
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kStageBytes);
+    uint64_t* empty = full + S;
+    int* flag = reinterpret_cast<int*>(empty + S);
+    unsigned char* region = smem + S * kStageBytes + kHdrBytes;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int B = p.B;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    allow_dependents();
+
+    if (warp == W) {
+        // ---- producer: global chunk c goes to warp c % W, whose r-th chunk (r = c / W) uses stage
+        // (c % W) + (r % D) * W in round r / D.  Weights are read-only, so streaming may start
+        // before the previous kernel in the stream has finished.
+        if (lane == 0) {
+            uint32_t c = 0;
+            for (int i = 0; i < p.n_mats; ++i) {
+                const MatDesc& m = p.m[i];
+                Share s;
+                if (!cta_share<true>(m, blockIdx.x, s)) continue;
+                const int G = m.K >> 7;
+                const int cpt = (s.Gs + kKC - 1) / kKC;
+                for (int t0 = 0; t0 < s.T; t0 += m.tiles_per_pass) {
+                    const int tp = min(m.tiles_per_pass, s.T - t0);
+                    for (int lc = 0; lc < tp * cpt; ++lc, ++c) {
+                        const int tile = t0 + lc / cpt;
+                        const int kc = lc % cpt;
+                        const int ng = min(kKC, s.Gs - kc * kKC);
+                        const uint32_t r = c / W;
+                        const int slot = static_cast<int>(c % W) + static_cast<int>(r % D) * W;
+                        const uint32_t round = r / D;
+                        if (round > 0 && !mbar_wait(&empty[slot], (round & 1) ^ 1, p.wait_limit)) report_timeout();
+                        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(ng * kRecBytes));
+                        const uint8_t* src =
+                            m.tiled + (static_cast<size_t>(s.t0 + tile) * G + s.g0 + kc * kKC) * kRecBytes;
+                        bulk_g2s(ring + slot * kStageBytes, src, static_cast<uint32_t>(ng * kRecBytes), &full[slot]);
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ---- consumers
+    grid_dependency_wait();  // x may be the previous kernel's output; y and ws are shared with it
+    constexpr int NT = W * 32;
+    const int tid = threadIdx.x;
+    const int q = lane >> 2, t = lane & 3;
+    uint32_t c = 0;  // global chunk counter, as in the producer
+    for (int i = 0; i < p.n_mats; ++i) {
+        const MatDesc& m = p.m[i];
+        Share s;
+        if (!cta_share<true>(m, blockIdx.x, s)) continue;
+        const int cpt = (s.Gs + kKC - 1) / kKC;
+        uint2* xs = reinterpret_cast<uint2*>(region);
+        float* ssum = reinterpret_cast<float*>(region + static_cast<size_t>(s.Gs) * 256 * BT);
+        float* fac = ssum + s.Gs * 8;
+        unsigned* colmax = reinterpret_cast<unsigned*>(fac + 8);
+        float* part = reinterpret_cast<float*>(colmax + 8);
+        stage_x<BT>(m.x, m.K, B, s.g0, s.Gs, xs, ssum, fac, colmax, tid, NT, [] { consumer_sync<NT>(); });
+        consumer_sync<NT>();
+        const float f0 = fac[2 * t], f1 = fac[2 * t + 1];
+        for (int pass = 0, t0 = 0; t0 < s.T; ++pass, t0 += m.tiles_per_pass) {
+            const int tp = min(m.tiles_per_pass, s.T - t0);
+            const int prow0 = s.r0 + t0 * 16;
+            const int prows = min(tp * 16, s.r1 - prow0);
+            const int nch = tp * cpt;
+            for (int lc = static_cast<int>((warp + W - c % W) % W); lc < nch; lc += W) {
+                const uint32_t cc_g = c + lc;
+                const uint32_t r = cc_g / W;
+                const int slot = warp + static_cast<int>(r % D) * W;
+                if (!mbar_wait(&full[slot], (r / D) & 1, p.wait_limit)) report_timeout();
+                const int jj = lc / cpt;
+                const int kc = lc - jj * cpt;
+                const int ng = min(kKC, s.Gs - kc * kKC);
+                const unsigned char* stg = ring + slot * kStageBytes;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int gl = kc * kKC + gi;
+                    const unsigned char* rec = stg + gi * kRecBytes;
+                    const uint4 qa = lds128(rec + 16 * lane);
+                    const uint4 qb = lds128(rec + 512 + 16 * lane);
+                    const uint2 sc = lds64(rec + 1024 + 8 * q);
+                    float cc[4];
+                    group_dot<MMA, BT>(qa, qb, xs + xfrag_index<BT>(gl, 0, 0), lane, B, cc);
+                    group_epilogue(acc, cc, sc.x, sc.y, ssum + gl * 8 + 2 * t, f0, f1);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);  // release: the reads above are done
+                float* pp = part + static_cast<size_t>(lc) * 16 * B;
+                const int c0 = 2 * t, c1 = 2 * t + 1;
+                if (c0 < B) { pp[q * B + c0] = acc[0]; pp[(q + 8) * B + c0] = acc[2]; }
+                if (c1 < B) { pp[q * B + c1] = acc[1]; pp[(q + 8) * B + c1] = acc[3]; }
+            }
+            c += nch;
+            consumer_sync<NT>();
+            // add the chunk partials of each row in chunk order
+            for (int idx = tid; idx < prows * B; idx += NT) {
+                const int b = idx / prows;
+                const int rr = idx - b * prows;
+                const int jj = rr >> 4, rl = rr & 15;
+                float sum = 0.f;
+                for (int kc = 0; kc < cpt; ++kc) sum += part[((jj * cpt + kc) * 16 + rl) * B + b];
+                store_row_sum(m, s, b, prow0 + rr, B, sum);
+            }
+            finish_rows<NT>(m, s, pass, prow0, prows, B, tid, flag, [] { consumer_sync<NT>(); });
+            consumer_sync<NT>();  // partials, x and flag may be overwritten from here on
+        }
+    }
+}
+
+// ================================================================== activation prep + tile kernel
+// q4_xprep_kernel: one CTA per matrix stages its activations once, in global memory, exactly as
+// stage_x does in shared memory for the kernels above: x in B-fragment order scaled per column,
+// the per-group sums of x and the per-column factors.
+struct PrepJob {
+    const uint16_t* x;
+    uint2* xf;
+    float* S;
+    float* fac;
+    int K;
+    int pad;
+};
+
+struct PrepParams {
+    int n;
+    int B;
+    PrepJob j[kMaxMats];
+};
+
+template <int BT>
+__global__ void __launch_bounds__(256) q4_xprep_kernel(const __grid_constant__ PrepParams p) {
+    __shared__ unsigned colmax[8];
+    grid_dependency_wait();  // x may be the previous kernel's output
+    allow_dependents();
+    const PrepJob& j = p.j[blockIdx.x];
+    stage_x<BT>(j.x, j.K, p.B, 0, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, 256, [] { __syncthreads(); });
+}
+
+// q4_tiles_kernel: one CTA per SM, persistent over a list of independent matrices, no block-wide
+// barrier after the start.  CTA c owns one row block of every matrix (rotated per matrix); its
+// tiles, matrix after matrix, form one list that the warps take from a shared counter.  A warp
+// computes a whole 16-row tile: all K/128 groups in order, codes from the L1 records with DEPTH
+// records in registers and `l2_ahead` more requested from L2, activations from the prepared
+// global copy, the sum kept in registers, Y written by the warp.  Which warp takes which tile
+// does not change any arithmetic.
+struct TileMat {
+    const uint8_t* tiled;
+    const uint2* xf;
+    const float* S;
+    const float* fac;
+    float* y;
+    int N, K;
+    int row_blocks, rot;
+};
+
+struct TileParams {
+    int n_mats;
+    int B;
+    int l2_ahead;
+    int pad;
+    TileMat m[kMaxMats];
+};
+
+template <int WARPS, int DEPTH, int BT>
+__global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_kernel(const __grid_constant__ TileParams p) {
+    __shared__ int prefix[kMaxMats + 1];  // this CTA's tiles in matrices [0, i)
+    __shared__ int tfirst[kMaxMats];      // first tile of this CTA's row block in matrix i
+    __shared__ int next_item;
+    const int lane = threadIdx.x & 31;
+    const int t = lane & 3, q = lane >> 2;
+    const int B = p.B;
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int i = 0; i < p.n_mats; ++i) {
+            const TileMat& m = p.m[i];
+            prefix[i] = acc;
+            tfirst[i] = 0;
+            if (static_cast<int>(blockIdx.x) < m.row_blocks) {
+                const int T_all = (m.N + 15) >> 4;
+                const int rb = (static_cast<int>(blockIdx.x) + m.rot) % m.row_blocks;
+                const int t0 = static_cast<int>(static_cast<int64_t>(rb) * T_all / m.row_blocks);
+                const int t1 = static_cast<int>(static_cast<int64_t>(rb + 1) * T_all / m.row_blocks);
+                tfirst[i] = t0;
+                acc += t1 - t0;
+            }
+        }
+        prefix[p.n_mats] = acc;
+        next_item = 0;
+    }
+    __syncthreads();
+    const int total = prefix[p.n_mats];
+    bool waited = false;
+    int mi = 0;  // matrix cursor: items only increase, so it only moves forward
+    for (;;) {
+        int item = 0;
+        if (lane == 0) item = atomicAdd(&next_item, 1);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= total) break;
+        while (prefix[mi + 1] <= item) ++mi;
+        const TileMat& m = p.m[mi];
+        const int G = m.K >> 7;
+        const int tile = tfirst[mi] + (item - prefix[mi]);
+        const uint8_t* rec0 = m.tiled + static_cast<size_t>(tile) * G * kRecBytes;
+        // records DEPTH .. DEPTH + l2_ahead - 1 to L2, the first DEPTH into registers
+        if (lane == 0 && p.l2_ahead > 0 && G > DEPTH)
+            prefetch_l2_bulk(rec0 + DEPTH * kRecBytes, static_cast<uint32_t>(min(p.l2_ahead, G - DEPTH) * kRecBytes));
+        Stage st[DEPTH];
+#pragma unroll
+        for (int d = 0; d < DEPTH; ++d) {
+            const uint8_t* r = rec0 + static_cast<size_t>(min(d, G - 1)) * kRecBytes;
+            st[d].qa = ld_stream_u4(r + 16 * lane);
+            st[d].qb = ld_stream_u4(r + 512 + 16 * lane);
+            const uint2 v = ld_stream_u2(r + 1024 + 8 * q);
+            st[d].sa_ma = v.x;
+            st[d].sb_mb = v.y;
+        }
+        if (!waited) {
+            grid_dependency_wait();  // the prepared activations come from the kernel before
+            allow_dependents();
+            waited = true;
+        }
+        const float f0 = ld_dep_f32(m.fac + 2 * t), f1 = ld_dep_f32(m.fac + 2 * t + 1);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        auto step = [&](int gg, Stage& slot) {
+            const Stage cur = slot;
+            // refill with the record DEPTH ahead (the last one again near the end: an L1/L2 hit)
+            const int gn = min(gg + DEPTH, G - 1);
+            const uint8_t* r = rec0 + static_cast<size_t>(gn) * kRecBytes;
+            if (lane == 0 && p.l2_ahead > 0 && gg + DEPTH + p.l2_ahead < G)
+                prefetch_l2_bulk(r + static_cast<size_t>(p.l2_ahead) * kRecBytes, kRecBytes);
+            slot.qa = ld_stream_u4(r + 16 * lane);
+            slot.qb = ld_stream_u4(r + 512 + 16 * lane);
+            const uint2 v = ld_stream_u2(r + 1024 + 8 * q);
+            slot.sa_ma = v.x;
+            slot.sb_mb = v.y;
+            float cc[4];
+            group_dot<true, BT, true>(cur.qa, cur.qb, m.xf + xfrag_index<BT>(gg, 0, 0), lane, B, cc);
+            group_epilogue<true>(acc, cc, cur.sa_ma, cur.sb_mb, m.S + gg * 8 + 2 * t, f0, f1);
+        };
+        int g = 0;
+        for (; g + DEPTH <= G; g += DEPTH) {
+#pragma unroll
+            for (int d = 0; d < DEPTH; ++d) step(g + d, st[d]);
+        }
+#pragma unroll
+        for (int d = 0; d < DEPTH; ++d)
+            if (g + d < G) step(g + d, st[d]);
+        const int ra = 16 * tile + q, rbw = ra + 8;
+        const int c0 = 2 * t, c1 = 2 * t + 1;
+        if (ra < m.N) {
+            if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + ra] = acc[0];
+            if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + ra] = acc[1];
+        }
+        if (rbw < m.N) {
+            if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + rbw] = acc[2];
+            if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + rbw] = acc[3];
+        }
+    }
+    if (!waited) {
+        grid_dependency_wait();
+        allow_dependents();
+    }
+}
+
+// ================================================================== argmax
 __device__ __forceinline__ bool ranks_above(float v, int i, float bv, int bi) {
     const bool vn = v != v, bn = bv != bv;
     if (vn || bn) return vn && (!bn || i < bi);
@@ -417,7 +1052,7 @@ __global__ void __launch_bounds__(1024) q4_argmax_kernel(const float* __restrict
     float bv = -__int_as_float(0x7f800000);
     int bi = 0x7fffffff;
     for (int i = threadIdx.x; i < N; i += blockDim.x) {
-        const float v = __ldg(row + i);
+        const float v = ld_dep_f32(row + i);
         if (ranks_above(v, i, bv, bi)) { bv = v; bi = i; }
     }
     for (int o = 16; o > 0; o >>= 1) {
@@ -443,13 +1078,7 @@ __global__ void __launch_bounds__(1024) q4_argmax_kernel(const float* __restrict
     }
 }
 
-// ------------------------------------------------------------------ host: plan
-struct Plan {
-    int row_blocks, k_splits, warps, depth, smax, kernel, sms, l2_prefetch;
-    bool pdl;
-    int Gs_max;
-};
-
+// ================================================================== host
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
     if (!v || !*v) return dflt;
@@ -470,50 +1099,131 @@ int device_sm_count(int* dev_out) {
     return cache[dev] > 0 ? cache[dev] : -1;
 }
 
-size_t plan_smem(const Plan& p, int B) {
-    return static_cast<size_t>(p.Gs_max) * 256 * B + static_cast<size_t>(p.Gs_max) * 32 +
-           static_cast<size_t>(p.warps) * p.smax * 16 * B * 4;
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Kernel choice and shape knobs: fixed defaults, overridable for benchmarking only.
+// kernel: 0 direct on L1 + tensor cores (default), 1 direct on L0 + tensor cores,
+//         2 direct on L0 + CUDA cores, 3 stream on L1 + tensor cores, 4 direct on L1 + CUDA cores.
+struct Knobs {
+    int kernel;
+    int warps, depth;  // direct kernel
+    int sw, sd;        // stream kernel: consumer warps, ring stages per consumer warp
+    int ksplit_min;
+    bool pdl, rotate;
+    int l2_ahead;      // direct kernel on L1: units prefetched into L2 ahead of the loads
+};
+
+Knobs knobs() {
+    Knobs k{};
+    k.kernel = env_int("Q4_KERNEL", -1);  // -1: chosen per call
+    if (k.kernel < -1 || k.kernel > 5) k.kernel = -1;
+    k.warps = env_int("Q4_WARPS", 16);
+    k.depth = env_int("Q4_DEPTH", 4);
+    const bool ok = (k.warps == 16 && (k.depth == 2 || k.depth == 4 || k.depth == 6)) ||
+                    (k.warps == 8 && (k.depth == 4 || k.depth == 8));
+    if (!ok || k.kernel == 2 || k.kernel == 4) { k.warps = 16; k.depth = 4; }
+    k.sw = env_int("Q4_SW", 8);
+    k.sd = env_int("Q4_SD", 2);
+    const bool sok = (k.sw == 8 && (k.sd == 1 || k.sd == 2)) || (k.sw == 4 && k.sd == 4) || (k.sw == 6 && k.sd == 2);
+    if (!sok) { k.sw = 8; k.sd = 2; }
+    k.ksplit_min = env_int("Q4_KSPLIT", 0);
+    k.pdl = env_int("Q4_PDL", 1) != 0;
+    k.rotate = env_int("Q4_ROTATE", 1) != 0;
+    k.l2_ahead = env_int("Q4_L2_AHEAD", 8);
+    if (k.l2_ahead < 0 || k.l2_ahead > 64) k.l2_ahead = 8;
+    return k;
 }
 
-// The split depends on (N, K, SM count) and on benchmarking overrides only.
-bool make_plan(int64_t N, int64_t K, int sms, Plan* out) {
+bool uses_l1(int kernel) { return kernel == 0 || kernel == 3 || kernel == 4 || kernel == 5; }
+bool is_stream(int kernel) { return kernel == 3; }
+bool is_tiles(int kernel) { return kernel == 5; }
+
+// Workspace of the tile kernel: the prepared activations of one matrix (x fragments, group
+// sums, column factors), for batch tile bt.
+size_t prep_bytes(int64_t K, int bt) {
+    const size_t G = static_cast<size_t>(K / 128);
+    return align256(G * 256 * bt + G * 32 + 32);
+}
+
+// The split of one (N, K) matrix.  Depends on N, K, the SM count and the kernel -- never on B.
+struct Plan {
+    int row_blocks, k_splits;
+    int gs_max;             // groups per CTA (largest k-slice)
+    int tiles_per_pass;     // stream: tiles whose chunk partials fit in shared memory at once
+    int passes;             // stream: passes of the largest row block
+    int smax;               // direct: most tiles one warp's range can touch
+};
+
+size_t ring_bytes(const Knobs& k) { return static_cast<size_t>(k.sw) * k.sd * kStageBytes + kHdrBytes; }
+
+bool default_shape(const Knobs& k) { return k.warps == 16 && k.depth == 4; }
+
+// Batch tile of the instantiation that runs batch B: the next power of two, or 8 for the
+// non-default direct shapes (instantiated for 8 columns only).
+int batch_tile(const Knobs& k, int kernel, int B) {
+    const int bt = B <= 1 ? 1 : (B <= 2 ? 2 : (B <= 4 ? 4 : 8));
+    if (kernel == 5) return bt;
+    if (is_stream(kernel)) return (k.sw == 8 && k.sd == 2) ? bt : 8;
+    return default_shape(k) ? bt : 8;
+}
+
+size_t plan_smem(const Knobs& k, int kernel, const Plan& p, int B) {
+    const int bt = batch_tile(k, kernel, B);
+    const size_t xs = static_cast<size_t>(p.gs_max) * 256 * bt + static_cast<size_t>(p.gs_max) * 32 + 64;
+    if (is_stream(kernel)) {
+        const int cpt = (p.gs_max + kKC - 1) / kKC;
+        return ring_bytes(k) + xs + static_cast<size_t>(p.tiles_per_pass) * cpt * 16 * B * 4;
+    }
+    return xs + static_cast<size_t>(k.warps) * p.smax * 16 * B * 4;
+}
+
+bool make_plan(int64_t N, int64_t K, int sms, const Knobs& k, int kernel, Plan* out) {
     Plan p{};
     const int G = static_cast<int>(K / 128);
-    p.sms = sms;
-    p.kernel = env_int("Q4_KERNEL", 0) == 1 ? 1 : 0;
-    p.warps = env_int("Q4_WARPS", 16);
-    p.depth = env_int("Q4_DEPTH", 4);
-    if (p.kernel == 1) p.depth = 4;
-    const bool ok_shape = (p.warps == 16 && (p.depth == 2 || p.depth == 4 || p.depth == 6)) ||
-                          (p.warps == 8 && (p.depth == 4 || p.depth == 8)) ||
-                          (p.warps == 32 && p.depth == 2);
-    if (!ok_shape || (p.kernel == 1 && p.warps != 16)) { p.warps = 16; p.depth = 4; }
-    p.pdl = env_int("Q4_PDL", 1) != 0;
-    p.l2_prefetch = env_int("Q4_L2_PREFETCH", 0);
-    // x for 8 columns of a k-slice takes 16 bytes per column of K in shared memory
-    int ks = static_cast<int>((K + 8191) / 8192);
-    const int ks_env = env_int("Q4_KSPLIT", 0);
-    if (ks_env > 0) ks = ks_env;
+    const int64_t T_all = (N + 15) / 16;
+    if (is_tiles(kernel)) {
+        p.row_blocks = static_cast<int>(T_all < sms ? T_all : sms);
+        p.k_splits = 1;
+        p.gs_max = G;
+        p.passes = 1;
+        *out = p;
+        return true;
+    }
+    int ks = k.ksplit_min > 0 ? k.ksplit_min : 1;
     if (ks > G) ks = G;
-    if (ks < 1) ks = 1;
     for (;; ++ks) {
+        if (ks > G) return false;
         int rb_max = sms / ks;
         if (rb_max < 1) rb_max = 1;
-        const int64_t tiles = (N + 15) / 16;
-        p.row_blocks = static_cast<int>(tiles < rb_max ? tiles : rb_max);
+        p.row_blocks = static_cast<int>(T_all < rb_max ? T_all : rb_max);
         p.k_splits = ks;
-        const int64_t rows_max = (N + p.row_blocks - 1) / p.row_blocks;
+        const int64_t rows_max =
+            uses_l1(kernel) ? 16 * ((T_all + p.row_blocks - 1) / p.row_blocks) : (N + p.row_blocks - 1) / p.row_blocks;
         const int Tm = static_cast<int>((rows_max + 15) / 16);
+        p.gs_max = (G + ks - 1) / ks;
         const int gs_min = G / ks;
-        p.Gs_max = (G + ks - 1) / ks;
-        const int64_t Um = static_cast<int64_t>(Tm) * p.Gs_max;
-        const int upw = static_cast<int>((Um + p.warps - 1) / p.warps);
-        int smax = (upw + gs_min - 1) / gs_min + 1;
-        if (smax > Tm) smax = Tm;
-        if (smax < 1) smax = 1;
-        p.smax = smax;
-        if (plan_smem(p, kMaxB) <= kSmemLimit) break;
-        if (ks >= G) return false;
+        p.passes = 1;
+        if (is_stream(kernel)) {
+            const int cpt = (p.gs_max + kKC - 1) / kKC;
+            const size_t fixed = ring_bytes(k) + static_cast<size_t>(p.gs_max) * (256 * kMaxB + 32) + 64;
+            const size_t per_tile = static_cast<size_t>(cpt) * 16 * kMaxB * 4;
+            if (fixed + per_tile > kSmemLimit) continue;
+            size_t tpp = (kSmemLimit - fixed) / per_tile;
+            if (tpp > static_cast<size_t>(Tm)) tpp = Tm;
+            p.tiles_per_pass = static_cast<int>(tpp);
+            p.passes = (Tm + p.tiles_per_pass - 1) / p.tiles_per_pass;
+            p.smax = 0;
+        } else {
+            const int64_t Um = static_cast<int64_t>(Tm) * p.gs_max;
+            const int upw = static_cast<int>((Um + k.warps - 1) / k.warps);
+            int smax = (upw + gs_min - 1) / gs_min + 1;
+            if (smax > Tm) smax = Tm;
+            if (smax < 1) smax = 1;
+            p.smax = smax;
+            p.tiles_per_pass = 0;
+            if (plan_smem(k, kernel, p, kMaxB) > kSmemLimit) continue;
+        }
+        break;
     }
     *out = p;
     return true;
@@ -521,34 +1231,32 @@ bool make_plan(int64_t N, int64_t K, int sms, Plan* out) {
 
 size_t plan_ws_bytes(const Plan& p, int64_t N, int B) {
     if (p.k_splits <= 1) return 0;
-    const size_t cnt = (static_cast<size_t>(p.row_blocks) * 4 + 255) / 256 * 256;
-    return cnt + static_cast<size_t>(p.k_splits) * B * N * 4;
+    return align256(static_cast<size_t>(p.row_blocks) * p.passes * 4) + static_cast<size_t>(p.k_splits) * B * N * 4;
 }
 
-using KernelFn = void (*)(GemvArgs);
-
-KernelFn pick_kernel(const Plan& p, int B) {
-    if (p.kernel == 1) {
-        if (B <= 1) return q4_gemv_kernel<16, 4, false, 1>;
-        if (B <= 2) return q4_gemv_kernel<16, 4, false, 2>;
-        if (B <= 4) return q4_gemv_kernel<16, 4, false, 4>;
-        return q4_gemv_kernel<16, 4, false, 8>;
-    }
-    if (p.warps == 8) return p.depth == 8 ? q4_gemv_kernel<8, 8, true, 8> : q4_gemv_kernel<8, 4, true, 8>;
-    if (p.warps == 32) return q4_gemv_kernel<32, 2, true, 8>;
-    if (p.depth == 2) return q4_gemv_kernel<16, 2, true, 8>;
-    if (p.depth == 6) return q4_gemv_kernel<16, 6, true, 8>;
-    return q4_gemv_kernel<16, 4, true, 8>;
+size_t job_ws_bytes(const Knobs& k, int kernel, const Plan& p, int64_t N, int64_t K, int B) {
+    if (is_tiles(kernel)) return prep_bytes(K, batch_tile(k, kernel, B));
+    return align256(plan_ws_bytes(p, N, B));
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool has_l0(const q4_matrix& W) { return W.codes && W.scales && W.mins; }
+
+q4_status check_shape(int64_t N, int64_t K) {
+    if (N <= 0) return Q4_ERR_INVALID_ARG;
+    if (N > 0x7fffffffLL) return Q4_ERR_UNSUPPORTED_SHAPE;
+    if (K <= 0 || K % 128 != 0 || K > kMaxK) return Q4_ERR_UNSUPPORTED_SHAPE;
+    return Q4_OK;
+}
 
 q4_status check_matrix(const q4_matrix* W) {
-    if (!W || !W->codes || !W->scales || !W->mins) return Q4_ERR_INVALID_ARG;
-    if (W->N <= 0) return Q4_ERR_INVALID_ARG;
-    if (W->N > 0x7fffffffLL) return Q4_ERR_UNSUPPORTED_SHAPE;
-    if (W->K <= 0 || W->K % 128 != 0 || W->K > kMaxK) return Q4_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned(W->codes, 16) || !aligned(W->scales, 2) || !aligned(W->mins, 2)) return Q4_ERR_MISALIGNED;
+    if (!W) return Q4_ERR_INVALID_ARG;
+    if (!has_l0(*W) && !W->tiled) return Q4_ERR_INVALID_ARG;
+    const q4_status s = check_shape(W->N, W->K);
+    if (s != Q4_OK) return s;
+    if (has_l0(*W) && (!aligned(W->codes, 16) || !aligned(W->scales, 2) || !aligned(W->mins, 2)))
+        return Q4_ERR_MISALIGNED;
+    if (W->tiled && !aligned(W->tiled, 16)) return Q4_ERR_MISALIGNED;
     return Q4_OK;
 }
 
@@ -564,102 +1272,367 @@ bool fault_injected() {
     return v && std::strcmp(v, "launch") == 0;
 }
 
-bool smem_attr_set(KernelFn fn, int dev) {
+template <typename Fn>
+bool smem_attr_set(Fn fn, int dev) {
     // cudaFuncSetAttribute once per (kernel, device)
-    struct Entry { KernelFn fn; int dev; };
-    static Entry done[256];
+    struct Entry {
+        const void* fn;
+        int dev;
+    };
+    static Entry done[512];
     static int n_done = 0;
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
+    const void* key = reinterpret_cast<const void*>(fn);
     for (int i = 0; i < n_done; ++i)
-        if (done[i].fn == fn && done[i].dev == dev) return true;
+        if (done[i].fn == key && done[i].dev == dev) return true;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit)) !=
         cudaSuccess)
         return false;
-    if (n_done < 256) done[n_done++] = Entry{fn, dev};
+    if (n_done < 512) done[n_done++] = Entry{key, dev};
     return true;
 }
 
-q4_status launch_gemv(const q4_matrix* W, const uint16_t* X, int B, float* Y, void* ws, const Plan& p,
-                      int dev, cudaStream_t stream) {
-    GemvArgs a{};
-    a.codes = W->codes;
-    a.scales = W->scales;
-    a.mins = W->mins;
-    a.x = X;
-    a.y = Y;
-    a.N = static_cast<int>(W->N);
-    a.K = static_cast<int>(W->K);
-    a.B = B;
-    a.row_blocks = p.row_blocks;
-    a.k_splits = p.k_splits;
-    a.smax = p.smax;
-    a.l2_prefetch = p.l2_prefetch;
-    if (p.k_splits > 1) {
-        const size_t cnt = (static_cast<size_t>(p.row_blocks) * 4 + 255) / 256 * 256;
-        a.ws_cnt = static_cast<unsigned int*>(ws);
-        a.ws_part = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + cnt);
-    }
+template <typename Fn, typename... Args>
+q4_status launch(Fn fn, int dev, unsigned grid, unsigned block, size_t smem, cudaStream_t stream, bool pdl,
+                 Args... args) {
     if (fault_injected()) return Q4_ERR_CUDA;
-    KernelFn fn = pick_kernel(p, B);
     if (!smem_attr_set(fn, dev)) return Q4_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.row_blocks * p.k_splits));
-    cfg.blockDim = dim3(static_cast<unsigned>(p.warps * 32));
-    cfg.dynamicSmemBytes = plan_smem(p, B);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fn, a) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, fn, args...) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+using KernelFn = void (*)(Params);
+
+template <int W, int DP, bool TL, bool MM>
+KernelFn direct_bt(int bt) {
+    switch (bt) {
+        case 1: return q4_direct_kernel<W, DP, TL, MM, 1>;
+        case 2: return q4_direct_kernel<W, DP, TL, MM, 2>;
+        case 4: return q4_direct_kernel<W, DP, TL, MM, 4>;
+        default: return q4_direct_kernel<W, DP, TL, MM, 8>;
+    }
+}
+
+KernelFn pick_kernel(const Knobs& k, int kernel, int B) {
+    const int bt = batch_tile(k, kernel, B);
+    switch (kernel) {
+        case 2: return direct_bt<16, 4, false, false>(bt);
+        case 4: return direct_bt<16, 4, true, false>(bt);
+        case 3:
+            if (k.sw == 8 && k.sd == 1) return q4_stream_kernel<8, 1, true, 8>;
+            if (k.sw == 4) return q4_stream_kernel<4, 4, true, 8>;
+            if (k.sw == 6) return q4_stream_kernel<6, 2, true, 8>;
+            switch (bt) {
+                case 1: return q4_stream_kernel<8, 2, true, 1>;
+                case 2: return q4_stream_kernel<8, 2, true, 2>;
+                case 4: return q4_stream_kernel<8, 2, true, 4>;
+                default: return q4_stream_kernel<8, 2, true, 8>;
+            }
+        case 1:
+            if (k.warps == 8) return k.depth == 8 ? q4_direct_kernel<8, 8, false, true, 8> : q4_direct_kernel<8, 4, false, true, 8>;
+            if (k.depth == 2) return q4_direct_kernel<16, 2, false, true, 8>;
+            if (k.depth == 6) return q4_direct_kernel<16, 6, false, true, 8>;
+            return direct_bt<16, 4, false, true>(bt);
+        default:
+            if (k.warps == 8) return k.depth == 8 ? q4_direct_kernel<8, 8, true, true, 8> : q4_direct_kernel<8, 4, true, true, 8>;
+            if (k.depth == 2) return q4_direct_kernel<16, 2, true, true, 8>;
+            if (k.depth == 6) return q4_direct_kernel<16, 6, true, true, 8>;
+            return direct_bt<16, 4, true, true>(bt);
+    }
+}
+
+unsigned block_threads(const Knobs& k, int kernel) {
+    return static_cast<unsigned>(is_stream(kernel) ? (k.sw + 1) * 32 : k.warps * 32);
+}
+
+// The kernel a list runs with: the requested one, moved to the other layout if the matrices
+// do not all carry the layout it reads.
+// The default: a list of independent matrices runs as one persistent tile-kernel launch (no
+// barrier between matrices); a single matrix, or a list whose launches must follow one another,
+// runs the direct kernel on the tiled copy, which splits K across the warps of a CTA.
+int default_kernel(int n, bool independent) { return (independent && n > 1) ? 5 : 0; }
+
+q4_status effective_kernel(const Knobs& k, const q4_matrix* mats, int n, bool independent, int* kernel) {
+    bool all_l1 = true, all_l0 = true;
+    for (int i = 0; i < n; ++i) {
+        all_l1 = all_l1 && mats[i].tiled != nullptr;
+        all_l0 = all_l0 && has_l0(mats[i]);
+    }
+    int kn = k.kernel >= 0 ? k.kernel : default_kernel(n, independent);
+    if (uses_l1(kn) && !all_l1) kn = (kn == 4) ? 2 : 1;
+    if (!uses_l1(kn) && !all_l0) kn = (kn == 2) ? 4 : 0;
+    if (uses_l1(kn) ? !all_l1 : !all_l0) return Q4_ERR_INVALID_ARG;
+    *kernel = kn;
+    return Q4_OK;
+}
+
+unsigned wait_limit() {
+    const int v = env_int("Q4_WAIT_LIMIT", 0);
+    return v > 0 ? static_cast<unsigned>(v) : kDefaultWaitLimit;
+}
+
+// ---- tile kernel: activation prep and streaming as two launches
+// Prepared activations of matrix i live at ws + (sum of prep_bytes of the matrices before it)
+// (or at ws for every matrix when `shared` lists run one matrix per launch).
+q4_status tiles_prepare(const Knobs& k, const q4_matrix* mats, int n, const uint16_t* const* X, int B, void* ws,
+                        bool independent, int dev, cudaStream_t stream) {
+    const int bt = batch_tile(k, 5, B);
+    const int per_launch = independent ? kMaxMats : 1;
+    size_t off = 0;
+    for (int base = 0; base < n; base += per_launch) {
+        const int cnt = n - base < per_launch ? n - base : per_launch;
+        PrepParams pp;
+        std::memset(&pp, 0, sizeof pp);
+        pp.n = cnt;
+        pp.B = B;
+        for (int i = 0; i < cnt; ++i) {
+            const q4_matrix& W = mats[base + i];
+            const size_t G = static_cast<size_t>(W.K / 128);
+            unsigned char* w = static_cast<unsigned char*>(ws) + (independent ? off : 0);
+            if (independent) off += prep_bytes(W.K, bt);
+            PrepJob& j = pp.j[i];
+            j.x = X[base + i];
+            j.K = static_cast<int>(W.K);
+            j.xf = reinterpret_cast<uint2*>(w);
+            j.S = reinterpret_cast<float*>(w + G * 256 * bt);
+            j.fac = j.S + G * 8;
+        }
+        using PrepFn = void (*)(PrepParams);
+        const PrepFn pf = bt == 1 ? q4_xprep_kernel<1> : bt == 2 ? q4_xprep_kernel<2> : bt == 4 ? q4_xprep_kernel<4>
+                                                                                               : q4_xprep_kernel<8>;
+        const q4_status s = launch(pf, dev, static_cast<unsigned>(cnt), 256u, 0, stream, k.pdl, pp);
+        if (s != Q4_OK) return s;
+    }
+    return Q4_OK;
+}
+
+q4_status tiles_stream(const Knobs& k, const q4_matrix* mats, int n, float* const* Y, int B, const void* ws,
+                       bool independent, int dev, int sms, cudaStream_t stream) {
+    const int bt = batch_tile(k, 5, B);
+    const int per_launch = independent ? kMaxMats : 1;
+    size_t off = 0;
+    for (int base = 0; base < n; base += per_launch) {
+        const int cnt = n - base < per_launch ? n - base : per_launch;
+        TileParams tp;
+        std::memset(&tp, 0, sizeof tp);
+        tp.n_mats = cnt;
+        tp.B = B;
+        tp.l2_ahead = k.l2_ahead;
+        int grid = 1;
+        for (int i = 0; i < cnt; ++i) {
+            const q4_matrix& W = mats[base + i];
+            const size_t G = static_cast<size_t>(W.K / 128);
+            const unsigned char* w = static_cast<const unsigned char*>(ws) + (independent ? off : 0);
+            if (independent) off += prep_bytes(W.K, bt);
+            TileMat& m = tp.m[i];
+            m.tiled = static_cast<const uint8_t*>(W.tiled);
+            m.xf = reinterpret_cast<const uint2*>(w);
+            m.S = reinterpret_cast<const float*>(w + G * 256 * bt);
+            m.fac = m.S + G * 8;
+            m.y = Y[base + i];
+            m.N = static_cast<int>(W.N);
+            m.K = static_cast<int>(W.K);
+            const int64_t T_all = (W.N + 15) / 16;
+            m.row_blocks = static_cast<int>(T_all < sms ? T_all : sms);
+            m.rot = (k.rotate && independent) ? static_cast<int>((static_cast<int64_t>(base + i) * 37) % m.row_blocks)
+                                              : 0;
+            if (m.row_blocks > grid) grid = m.row_blocks;
+        }
+        using TilesFn = void (*)(TileParams);
+        TilesFn tf = nullptr;
+        if (k.depth == 2)
+            tf = bt == 1 ? q4_tiles_kernel<16, 2, 1> : bt == 2 ? q4_tiles_kernel<16, 2, 2>
+               : bt == 4 ? q4_tiles_kernel<16, 2, 4> : q4_tiles_kernel<16, 2, 8>;
+        else
+            tf = bt == 1 ? q4_tiles_kernel<16, 4, 1> : bt == 2 ? q4_tiles_kernel<16, 4, 2>
+               : bt == 4 ? q4_tiles_kernel<16, 4, 4> : q4_tiles_kernel<16, 4, 8>;
+        const q4_status s = launch(tf, dev, static_cast<unsigned>(grid), 16u * 32u, 0, stream, k.pdl, tp);
+        if (s != Q4_OK) return s;
+    }
+    return Q4_OK;
+}
+
+size_t step_prep_bytes(const int64_t* K, int n, int B) {
+    const Knobs k = knobs();
+    const int bt = batch_tile(k, 5, B);
+    size_t need = 0;
+    for (int i = 0; i < n; ++i) need += prep_bytes(K[i], bt);
+    return need;
+}
+
+// Validate a list, then enqueue it: one persistent launch per kMaxMats matrices when the list
+// is independent, else one launch per matrix (stream-ordered, so Y[i] may feed X[j], j > i).
+q4_status run(const q4_matrix* mats, int n, const uint16_t* const* X, float* const* Y, int B, void* ws,
+              size_t ws_bytes, bool independent, cudaStream_t stream) {
+    if (!mats || !X || !Y || n < 1) return Q4_ERR_INVALID_ARG;
+    if (B < 1 || B > kMaxB) return Q4_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        q4_status s = check_matrix(&mats[i]);
+        if (s != Q4_OK) return s;
+        if ((s = check_io(X[i], B, Y[i])) != Q4_OK) return s;
+    }
+    const Knobs k = knobs();
+    int kernel = 0;
+    q4_status st = effective_kernel(k, mats, n, independent, &kernel);
+    if (st != Q4_OK) return st;
+    int dev = 0;
+    const int sms = device_sm_count(&dev);
+    if (sms <= 0) return Q4_ERR_CUDA;
+    // plans and workspace: a persistent list gives every k-split matrix its own slice
+    size_t need = 0;
+    for (int i = 0; i < n; ++i) {
+        Plan pl;
+        if (!make_plan(mats[i].N, mats[i].K, sms, k, kernel, &pl)) return Q4_ERR_UNSUPPORTED_SHAPE;
+        const size_t b = job_ws_bytes(k, kernel, pl, mats[i].N, mats[i].K, B);
+        need = independent ? need + b : (b > need ? b : need);
+    }
+    if (need > 0) {
+        if (!ws || ws_bytes < need) return Q4_ERR_WORKSPACE;
+        if (!aligned(ws, 16)) return Q4_ERR_MISALIGNED;
+    }
+    const int per_launch = independent ? kMaxMats : 1;
+    if (is_tiles(kernel)) {
+        q4_status s2 = tiles_prepare(k, mats, n, X, B, ws, independent, dev, stream);
+        if (s2 != Q4_OK) return s2;
+        return tiles_stream(k, mats, n, Y, B, ws, independent, dev, sms, stream);
+    }
+    size_t off = 0;
+    for (int base = 0; base < n; base += per_launch) {
+        const int cnt = n - base < per_launch ? n - base : per_launch;
+        Params prm;
+        std::memset(&prm, 0, sizeof prm);
+        prm.n_mats = cnt;
+        prm.B = B;
+        prm.wait_limit = wait_limit();
+        prm.l2_ahead = k.l2_ahead;
+        size_t smem = 0;
+        int grid = 1;
+        for (int i = 0; i < cnt; ++i) {
+            const q4_matrix& W = mats[base + i];
+            Plan pl;
+            make_plan(W.N, W.K, sms, k, kernel, &pl);
+            MatDesc& m = prm.m[i];
+            m.codes = W.codes;
+            m.scales = W.scales;
+            m.mins = W.mins;
+            m.tiled = static_cast<const uint8_t*>(W.tiled);
+            m.x = X[base + i];
+            m.y = Y[base + i];
+            m.N = static_cast<int>(W.N);
+            m.K = static_cast<int>(W.K);
+            m.row_blocks = pl.row_blocks;
+            m.k_splits = pl.k_splits;
+            m.tiles_per_pass = pl.tiles_per_pass;
+            m.passes = pl.passes;
+            m.smax = pl.smax;
+            m.rot = (k.rotate && independent) ? static_cast<int>((static_cast<int64_t>(base + i) * 37) % pl.row_blocks) : 0;
+            if (pl.k_splits > 1) {
+                unsigned char* w = static_cast<unsigned char*>(ws) + (independent ? off : 0);
+                m.ws_cnt = reinterpret_cast<unsigned*>(w);
+                m.ws_part = reinterpret_cast<float*>(w + align256(static_cast<size_t>(pl.row_blocks) * pl.passes * 4));
+                if (independent) off += align256(plan_ws_bytes(pl, W.N, B));
+            }
+            const size_t sm = plan_smem(k, kernel, pl, B);
+            if (sm > smem) smem = sm;
+            if (pl.row_blocks * pl.k_splits > grid) grid = pl.row_blocks * pl.k_splits;
+        }
+        if (smem > kSmemLimit) return Q4_ERR_UNSUPPORTED_SHAPE;
+        const q4_status s = launch(pick_kernel(k, kernel, B), dev, static_cast<unsigned>(grid),
+                                   block_threads(k, kernel), smem, stream, k.pdl, prm);
+        if (s != Q4_OK) return s;
+    }
+    return Q4_OK;
+}
+
+// The split (and so the workspace) depends on the kernel family only through the shared-memory
+// budget that decides k_splits; the layout (row vs tile grain) does not change it.
+size_t workspace_for(const int64_t* N, const int64_t* K, int n, int B, bool independent) {
+    if (n < 1 || B < 1 || B > kMaxB) return 0;
+    const int sms = device_sm_count(nullptr);
+    if (sms <= 0) return 0;
+    const Knobs k = knobs();
+    const int kernel = k.kernel >= 0 ? k.kernel : default_kernel(n, independent);
+    size_t need = 0;
+    for (int i = 0; i < n; ++i) {
+        if (check_shape(N[i], K[i]) != Q4_OK) return 0;
+        Plan p;
+        if (!make_plan(N[i], K[i], sms, k, kernel, &p)) return 0;
+        const size_t b = job_ws_bytes(k, kernel, p, N[i], K[i], B);
+        need = independent ? need + b : (b > need ? b : need);
+    }
+    return need;
 }
 
 }  // namespace
 
 // ------------------------------------------------------------------ C ABI
+extern "C" size_t q4_tiled_bytes(int64_t N, int64_t K) {
+    if (check_shape(N, K) != Q4_OK) return 0;
+    return static_cast<size_t>((N + 15) / 16) * static_cast<size_t>(K / 128) * kRecBytes;
+}
+
+extern "C" q4_status q4_tile(const q4_matrix* W, void* tiled, size_t tiled_bytes, void* stream) {
+    if (!W || !has_l0(*W) || !tiled) return Q4_ERR_INVALID_ARG;
+    q4_status s = check_shape(W->N, W->K);
+    if (s != Q4_OK) return s;
+    if (!aligned(W->codes, 16) || !aligned(W->scales, 2) || !aligned(W->mins, 2) || !aligned(tiled, 16))
+        return Q4_ERR_MISALIGNED;
+    if (tiled_bytes < q4_tiled_bytes(W->N, W->K)) return Q4_ERR_WORKSPACE;
+    if (fault_injected()) return Q4_ERR_CUDA;
+    const int64_t pieces = ((W->N + 15) / 16) * (W->K / 128) * 68;
+    const unsigned grid = static_cast<unsigned>((pieces + 255) / 256);
+    q4_tile_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        W->codes, W->scales, W->mins, static_cast<int>(W->N), static_cast<int>(W->K), static_cast<uint8_t*>(tiled),
+        pieces);
+    return cudaPeekAtLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
 extern "C" size_t q4_workspace_bytes(int64_t N, int64_t K, int B) {
-    if (N <= 0 || N > 0x7fffffffLL || K <= 0 || K % 128 || K > kMaxK || B < 1 || B > kMaxB) return 0;
-    const int sms = device_sm_count(nullptr);
-    if (sms <= 0) return 0;
-    Plan p;
-    if (!make_plan(N, K, sms, &p)) return 0;
-    return plan_ws_bytes(p, N, B);
+    return workspace_for(&N, &K, 1, B, true);
+}
+
+extern "C" size_t q4_decode_step_workspace_bytes(const int64_t* N, const int64_t* K, int n_mats, int B,
+                                                 unsigned flags) {
+    if (!N || !K) return 0;
+    return workspace_for(N, K, n_mats, B, (flags & Q4_STEP_INDEPENDENT) != 0);
 }
 
 extern "C" q4_status q4_plan(int64_t N, int64_t K, q4_plan_info* out) {
-    if (!out || N <= 0) return Q4_ERR_INVALID_ARG;
-    if (N > 0x7fffffffLL || K <= 0 || K % 128 || K > kMaxK) return Q4_ERR_UNSUPPORTED_SHAPE;
+    if (!out) return Q4_ERR_INVALID_ARG;
+    const q4_status s = check_shape(N, K);
+    if (s != Q4_OK) return s;
     const int sms = device_sm_count(nullptr);
     if (sms <= 0) return Q4_ERR_CUDA;
+    Knobs k = knobs();
+    if (k.kernel < 0) k.kernel = default_kernel(1, true);
     Plan p;
-    if (!make_plan(N, K, sms, &p)) return Q4_ERR_UNSUPPORTED_SHAPE;
+    if (!make_plan(N, K, sms, k, k.kernel, &p)) return Q4_ERR_UNSUPPORTED_SHAPE;
     out->row_blocks = p.row_blocks;
     out->k_splits = p.k_splits;
-    out->warps_per_cta = p.warps;
-    out->prefetch_depth = p.depth;
-    out->kernel = p.kernel;
-    out->sm_count = p.sms;
+    out->warps_per_cta = is_tiles(k.kernel) ? 16 : static_cast<int32_t>(block_threads(k, k.kernel) / 32);
+    out->prefetch_depth = is_stream(k.kernel) ? k.sw * k.sd : k.depth;
+    out->kernel = k.kernel;
+    out->sm_count = sms;
     return Q4_OK;
 }
 
 extern "C" q4_status q4_gemm_skinny(const q4_matrix* W, const uint16_t* X, int B, float* Y, void* ws,
                                     size_t ws_bytes, void* stream) {
+    if (!W) return Q4_ERR_INVALID_ARG;
     q4_status s = check_matrix(W);
     if (s != Q4_OK) return s;
     if ((s = check_io(X, B, Y)) != Q4_OK) return s;
-    int dev = 0;
-    const int sms = device_sm_count(&dev);
-    if (sms <= 0) return Q4_ERR_CUDA;
-    Plan p;
-    if (!make_plan(W->N, W->K, sms, &p)) return Q4_ERR_UNSUPPORTED_SHAPE;
-    const size_t need = plan_ws_bytes(p, W->N, B);
-    if (need > 0) {
-        if (!ws || ws_bytes < need) return Q4_ERR_WORKSPACE;
-        if (!aligned(ws, 16)) return Q4_ERR_MISALIGNED;
-    }
-    return launch_gemv(W, X, B, Y, ws, p, dev, static_cast<cudaStream_t>(stream));
+    return run(W, 1, &X, &Y, B, ws, ws_bytes, true, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" q4_status q4_gemv(const q4_matrix* W, const uint16_t* x, float* y, void* ws, size_t ws_bytes,
@@ -668,33 +1641,60 @@ extern "C" q4_status q4_gemv(const q4_matrix* W, const uint16_t* x, float* y, vo
 }
 
 extern "C" q4_status q4_decode_step(const q4_matrix* mats, int n_mats, const uint16_t* const* X,
-                                    float* const* Y, int B, void* ws, size_t ws_bytes, void* stream) {
-    if (!mats || !X || !Y || n_mats < 1) return Q4_ERR_INVALID_ARG;
-    if (B < 1 || B > kMaxB) return Q4_ERR_INVALID_ARG;
-    int dev = 0;
-    const int sms = device_sm_count(&dev);
-    if (sms <= 0) return Q4_ERR_CUDA;
+                                    float* const* Y, int B, void* ws, size_t ws_bytes, unsigned flags,
+                                    void* stream) {
+    return run(mats, n_mats, X, Y, B, ws, ws_bytes, (flags & Q4_STEP_INDEPENDENT) != 0,
+               static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t q4_step_workspace_bytes(const int64_t* K, int n_mats, int B) {
+    if (!K || n_mats < 1 || B < 1 || B > kMaxB) return 0;
+    for (int i = 0; i < n_mats; ++i)
+        if (K[i] <= 0 || K[i] % 128 || K[i] > kMaxK) return 0;
+    return step_prep_bytes(K, n_mats, B);
+}
+
+// Shared checks of the two phases.
+static q4_status check_step(const q4_matrix* mats, int n, int B, const void* ws, size_t ws_bytes, int* dev, int* sms) {
+    if (!mats || n < 1 || B < 1 || B > kMaxB || !ws) return Q4_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        const q4_status s = check_matrix(&mats[i]);
+        if (s != Q4_OK) return s;
+        if (!mats[i].tiled) return Q4_ERR_INVALID_ARG;
+    }
+    if (!aligned(ws, 16)) return Q4_ERR_MISALIGNED;
     size_t need = 0;
+    const Knobs k = knobs();
+    for (int i = 0; i < n; ++i) need += prep_bytes(mats[i].K, batch_tile(k, 5, B));
+    if (ws_bytes < need) return Q4_ERR_WORKSPACE;
+    *sms = device_sm_count(dev);
+    return *sms > 0 ? Q4_OK : Q4_ERR_CUDA;
+}
+
+extern "C" q4_status q4_step_prepare(const q4_matrix* mats, int n_mats, const uint16_t* const* X, int B, void* ws,
+                                     size_t ws_bytes, void* stream) {
+    int dev = 0, sms = 0;
+    q4_status s = check_step(mats, n_mats, B, ws, ws_bytes, &dev, &sms);
+    if (s != Q4_OK) return s;
+    if (!X) return Q4_ERR_INVALID_ARG;
     for (int i = 0; i < n_mats; ++i) {
-        q4_status s = check_matrix(&mats[i]);
-        if (s != Q4_OK) return s;
-        if ((s = check_io(X[i], B, Y[i])) != Q4_OK) return s;
-        Plan p;
-        if (!make_plan(mats[i].N, mats[i].K, sms, &p)) return Q4_ERR_UNSUPPORTED_SHAPE;
-        const size_t n = plan_ws_bytes(p, mats[i].N, B);
-        if (n > need) need = n;
+        if (!X[i]) return Q4_ERR_INVALID_ARG;
+        if (!aligned(X[i], 16)) return Q4_ERR_MISALIGNED;
     }
-    if (need > 0) {
-        if (!ws || ws_bytes < need) return Q4_ERR_WORKSPACE;
-        if (!aligned(ws, 16)) return Q4_ERR_MISALIGNED;
-    }
+    return tiles_prepare(knobs(), mats, n_mats, X, B, ws, true, dev, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" q4_status q4_step_stream(const q4_matrix* mats, int n_mats, float* const* Y, int B, const void* ws,
+                                    size_t ws_bytes, void* stream) {
+    int dev = 0, sms = 0;
+    q4_status s = check_step(mats, n_mats, B, ws, ws_bytes, &dev, &sms);
+    if (s != Q4_OK) return s;
+    if (!Y) return Q4_ERR_INVALID_ARG;
     for (int i = 0; i < n_mats; ++i) {
-        Plan p;
-        make_plan(mats[i].N, mats[i].K, sms, &p);
-        const q4_status s = launch_gemv(&mats[i], X[i], B, Y[i], ws, p, dev, static_cast<cudaStream_t>(stream));
-        if (s != Q4_OK) return s;
+        if (!Y[i]) return Q4_ERR_INVALID_ARG;
+        if (!aligned(Y[i], 4)) return Q4_ERR_MISALIGNED;
     }
-    return Q4_OK;
+    return tiles_stream(knobs(), mats, n_mats, Y, B, ws, true, dev, sms, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream) {
@@ -712,4 +1712,14 @@ extern "C" q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* id
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, q4_argmax_kernel, Y, static_cast<int>(N), idx) == cudaSuccess ? Q4_OK
                                                                                                 : Q4_ERR_CUDA;
+}
+
+extern "C" q4_status q4_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return Q4_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_q4_device_error, sizeof v) != cudaSuccess) return Q4_ERR_CUDA;
+    if (v == 0) return Q4_OK;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_q4_device_error, &zero, sizeof zero) != cudaSuccess) return Q4_ERR_CUDA;
+    return Q4_ERR_TIMEOUT;
 }

@@ -17,7 +17,9 @@ from int4_weight_only_q4_gb300 import _lib
 def test_library_exports_every_declared_function():
     names = _lib.header_functions()
     assert {"q4_pack_host", "q4_gemv", "q4_gemm_skinny", "q4_decode_step", "q4_argmax_f32",
-            "q4_workspace_bytes", "q4_plan", "q4_status_string"} <= set(names)
+            "q4_workspace_bytes", "q4_decode_step_workspace_bytes", "q4_plan", "q4_device_status",
+            "q4_tiled_bytes", "q4_tile", "q4_step_workspace_bytes", "q4_step_prepare", "q4_step_stream",
+            "q4_status_string"} <= set(names)
     for n in names:
         assert hasattr(_lib.lib, n), n
 
@@ -119,12 +121,37 @@ def test_host_validation_before_any_cuda_call():
     assert L.q4_gemv(ctypes.byref(m), 16, 16, None, 0, None) == _lib.Q4_ERR_UNSUPPORTED_SHAPE
     m = _lib.q4_matrix(16, 16, 16, 1 << 31, 256)
     assert L.q4_gemv(ctypes.byref(m), 16, 16, None, 0, None) == _lib.Q4_ERR_UNSUPPORTED_SHAPE
-    assert L.q4_decode_step(None, 1, None, None, 1, None, 0, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_decode_step(None, 1, None, None, 1, None, 0, 1, None) == _lib.Q4_ERR_INVALID_ARG
     arr = (_lib.q4_matrix * 1)(_lib.q4_matrix(16, 16, 16, 10, 256))
-    assert L.q4_decode_step(arr, 0, None, None, 1, None, 0, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_decode_step(arr, 0, None, None, 1, None, 0, 1, None) == _lib.Q4_ERR_INVALID_ARG
+    xp = (_lib.c_vp * 1)(16)
+    yp = (_lib.c_vp * 1)(16)
+    assert L.q4_decode_step(arr, 1, xp, yp, 9, None, 0, 0, None) == _lib.Q4_ERR_INVALID_ARG
+    bad = (_lib.q4_matrix * 1)(_lib.q4_matrix(16, 16, 16, 10, 200))
+    assert L.q4_decode_step(bad, 1, xp, yp, 1, None, 0, 1, None) == _lib.Q4_ERR_UNSUPPORTED_SHAPE
     assert L.q4_argmax_f32(16, 9, 10, 16, None) == _lib.Q4_ERR_INVALID_ARG
     assert L.q4_argmax_f32(16, 1, 0, 16, None) == _lib.Q4_ERR_INVALID_ARG
     assert L.q4_argmax_f32(None, 1, 10, 16, None) == _lib.Q4_ERR_INVALID_ARG
     assert L.q4_workspace_bytes(10, 200, 1) == 0
+    assert L.q4_tiled_bytes(10, 200) == 0
+    Ks = (_lib.c_i64 * 2)(3072, 200)
+    assert L.q4_step_workspace_bytes(Ks, 2, 1) == 0
+    assert L.q4_step_workspace_bytes(Ks, 1, 1) == (24 * (256 + 32) + 32 + 255) // 256 * 256
+    assert L.q4_step_workspace_bytes(Ks, 1, 9) == 0
+    assert L.q4_step_prepare(None, 1, None, 1, 16, 1 << 20, None) == _lib.Q4_ERR_INVALID_ARG
+    nt = (_lib.q4_matrix * 1)(_lib.q4_matrix(16, 16, 16, 10, 256))          # no tiled copy
+    assert L.q4_step_stream(nt, 1, None, 1, 16, 1 << 20, None) == _lib.Q4_ERR_INVALID_ARG
+    tt = (_lib.q4_matrix * 1)(_lib.q4_matrix(None, None, None, 10, 256, 16))
+    assert L.q4_step_stream(tt, 1, None, 1, 16, 8, None) == _lib.Q4_ERR_WORKSPACE
+    assert L.q4_step_stream(tt, 1, None, 1, 8, 1 << 20, None) == _lib.Q4_ERR_MISALIGNED
+    assert L.q4_tiled_bytes(17, 384) == 2 * 3 * 1088
+    assert L.q4_tile(None, 16, 1 << 20, None) == _lib.Q4_ERR_INVALID_ARG
+    m = _lib.q4_matrix(16, 16, 16, 17, 384)
+    assert L.q4_tile(ctypes.byref(m), 16, 100, None) == _lib.Q4_ERR_WORKSPACE
+    assert L.q4_tile(ctypes.byref(m), 8, 1 << 20, None) == _lib.Q4_ERR_MISALIGNED
+    m = _lib.q4_matrix(None, None, None, 17, 384, 16)      # tiled copy only: accepted by the checks
+    assert L.q4_gemv(ctypes.byref(m), 16, 16, None, 0, None) != _lib.Q4_ERR_INVALID_ARG
+    m = _lib.q4_matrix(None, None, None, 17, 384, 8)       # misaligned tiled copy
+    assert L.q4_gemv(ctypes.byref(m), 16, 16, None, 0, None) == _lib.Q4_ERR_MISALIGNED
     info = _lib.q4_plan_info()
     assert L.q4_plan(10, 200, ctypes.byref(info)) == _lib.Q4_ERR_UNSUPPORTED_SHAPE
