@@ -182,6 +182,19 @@ def profiled_traffic(kernel: str):
     return d.get("dram_bytes_per_launch", {}).get(kernel)
 
 
+def dist_max(value: float, device=None) -> float:
+    """Max of `value` over all ranks (the slowest rank sets the job's time); identity when not
+    distributed.  gloo reduces a CPU tensor, nccl a tensor on `device`."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -339,11 +352,7 @@ def run_ours(args):
         while time.time() < t_end:
             time_graph(g1, 200, 0)
     clocks = clk.summary()
-    ms1_t = torch.tensor([ms1], device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(ms1_t, op=dist.ReduceOp.MAX)
-    ms1 = float(ms1_t.item())
+    ms1 = dist_max(ms1, dev)
     ms8 = time_graph(graphs[8][0], max(20, args.steps // 4), max(3, args.warmup))
     sb1 = step_bytes(1)
     value = sb1 * world / (ms1 * 1e-3) / 1e9
