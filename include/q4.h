@@ -238,6 +238,37 @@ q4_status q4_step_stream(const q4_matrix* mats, int n_mats, float* const* Y, int
                          const void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * q4_gemm_skinny_noalloc -- Y = W X exactly as the tile kernel computes it
+ * (q4_step_prepare + q4_step_stream on a one-matrix list), for callers that
+ * cannot allocate device memory and so cannot supply a workspace: code that
+ * runs while a CUDA graph is being captured (cudaMalloc is not allowed there),
+ * real-time threads such as an audio callback that must never wait on the
+ * allocator (cudaMalloc/cudaFree can synchronise the device and take driver
+ * locks), and plugins or embedded hosts whose device memory is budgeted and
+ * owned by someone else.  The pages have no counterpart of this call.
+ *   W  as for q4_gemm_skinny, and it must carry the tiled copy;
+ *   X  device bf16 [B, K];  Y  device fp32 [B, N];  1 <= B <= 8.
+ * Scratch: a fixed q4_noalloc_scratch_bytes() = 512 KiB array inside the
+ * library, one per GPU that loads it, held until the process exits.  It holds
+ * the prepared activations, (K/128) * (256 * BT + 32) + 32 bytes with BT = B
+ * rounded up to 1, 2, 4 or 8: every K for B <= 2, K <= 63,488 for B <= 4 and
+ * K <= 32,256 for B <= 8.  Larger requests return Q4_ERR_WORKSPACE before
+ * anything is launched.  The call allocates nothing and frees nothing.
+ * All calls on a device share the one array and each leaves its contents
+ * behind (nothing in it needs to start at zero: every call rewrites what it
+ * reads).  Calls that overlap on the GPU -- on different streams, or from
+ * different host threads -- race on it; serialise them.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Other errors as for q4_gemm_skinny; Q4_ERR_CUDA if the lookup fails.
+ */
+q4_status q4_gemm_skinny_noalloc(const q4_matrix* W, const uint16_t* X, int B, float* Y,
+                                 void* stream);
+
+/* Size in bytes of q4_gemm_skinny_noalloc's fixed scratch array. */
+size_t q4_noalloc_scratch_bytes(void);
+
+/*
  * q4_argmax_f32 -- per batch row of logits Y [B, N] (device fp32), the index
  * of the largest value, the lowest index among equal maxima (NaN ranks above
  * every number, as numpy's argmax does), written to idx (device int32 [B]).

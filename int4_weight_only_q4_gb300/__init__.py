@@ -26,6 +26,7 @@ MAX_B = 8
 __all__ = ["GROUP", "MAX_B", "Q4Error", "QuantizedMatrix", "Workspace", "pack_host", "plan",
            "workspace_bytes", "decode_step_workspace_bytes", "tiled_bytes", "gemv", "gemm_skinny", "decode_step",
            "argmax", "device_status", "DecodeStepGraph", "step_workspace_bytes", "step_prepare", "step_stream",
+           "gemm_skinny_noalloc",
            "header_functions", "lib"]
 
 
@@ -166,6 +167,17 @@ def gemm_skinny(W: QuantizedMatrix, X: torch.Tensor, Y: torch.Tensor | None = No
     m = W.c_struct()
     st = lib.q4_gemm_skinny(ctypes.byref(m), _ptr(X), B, _ptr(Y), ws_p, ws_n, _stream_ptr(stream))
     check(st, "q4_gemm_skinny")
+    return Y
+
+
+def gemm_skinny_noalloc(W: QuantizedMatrix, X: torch.Tensor, Y: torch.Tensor, stream=None) -> torch.Tensor:
+    """Y = W X with no workspace: the library's fixed scratch array instead (see q4.h for its
+    limits and for the rule that calls overlapping on the GPU race)."""
+    X = _as_bf16(X)
+    B = 1 if X.dim() == 1 else X.shape[0]
+    m = W.c_struct()
+    check(lib.q4_gemm_skinny_noalloc(ctypes.byref(m), _ptr(X), B, _ptr(Y), _stream_ptr(stream)),
+          "q4_gemm_skinny_noalloc")
     return Y
 
 

@@ -1697,6 +1697,51 @@ extern "C" q4_status q4_step_stream(const q4_matrix* mats, int n_mats, float* co
     return tiles_stream(knobs(), mats, n_mats, Y, B, ws, true, dev, sms, static_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------------ no-allocation variant
+// Scratch of q4_gemm_skinny_noalloc: the prepared activations of one matrix, in device memory
+// that the library owns.  Every GPU that loads the library holds these 512 KiB until the process
+// exits.  Host code must not pass the symbol itself to a kernel (on the host it names a host-side
+// stand-in); the device address is looked up per device with cudaGetSymbolAddress.
+static constexpr size_t kNoallocScratchBytes = 512 * 1024;
+static __device__ __align__(256) unsigned char g_q4_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of the scratch on the current device, looked up once per device (with that
+// device current) on its first use; nullptr if the lookup failed.
+static void* noalloc_scratch(int dev) {
+    static void* addr[kMaxDevices];
+    static cudaError_t err[kMaxDevices];
+    static std::once_flag flags[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::call_once(flags[dev], [dev] {
+        void* p = nullptr;
+        err[dev] = cudaGetSymbolAddress(&p, g_q4_noalloc_scratch);
+        addr[dev] = err[dev] == cudaSuccess ? p : nullptr;
+    });
+    return addr[dev];
+}
+
+extern "C" size_t q4_noalloc_scratch_bytes(void) { return kNoallocScratchBytes; }
+
+extern "C" q4_status q4_gemm_skinny_noalloc(const q4_matrix* W, const uint16_t* X, int B, float* Y,
+                                            void* stream) {
+    if (!W) return Q4_ERR_INVALID_ARG;
+    q4_status s = check_matrix(W);
+    if (s != Q4_OK) return s;
+    if (!W->tiled) return Q4_ERR_INVALID_ARG;
+    if ((s = check_io(X, B, Y)) != Q4_OK) return s;
+    const Knobs k = knobs();
+    if (prep_bytes(W->K, batch_tile(k, 5, B)) > kNoallocScratchBytes) return Q4_ERR_WORKSPACE;
+    int dev = 0;
+    const int sms = device_sm_count(&dev);
+    if (sms <= 0) return Q4_ERR_CUDA;
+    void* scratch = noalloc_scratch(dev);
+    if (!scratch) return Q4_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = tiles_prepare(k, W, 1, &X, B, scratch, true, dev, st);
+    if (s != Q4_OK) return s;
+    return tiles_stream(k, W, 1, &Y, B, scratch, true, dev, sms, st);
+}
+
 extern "C" q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream) {
     if (!Y || !idx || B < 1 || B > kMaxB || N < 1 || N > 0x7fffffffLL) return Q4_ERR_INVALID_ARG;
     if (!aligned(Y, 4) || !aligned(idx, 4)) return Q4_ERR_MISALIGNED;
