@@ -422,9 +422,9 @@ def step_roofline(q4, torch, mats, g, dev, args):
     bytes_launch = sum(algo_bytes(N, K, 1) for N, K in step_shapes())
     achieved = bytes_launch / (avg_ms * 1e-3) / 1e9
     peak, src = measured_peak_gbs()
-    return {"bound": "hbm", "kernel": "q4_tiles_kernel (109 matrices of the step, B=1, one launch)",
+    return {"bound": "hbm", "kernel": "q4_tiles_ring_kernel (109 matrices of the step, B=1, one launch)",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic("q4_tiles_kernel"), "algorithmic_bytes_per_launch": bytes_launch,
+            "traffic": profiled_traffic("q4_tiles_ring_kernel"), "algorithmic_bytes_per_launch": bytes_launch,
             "avg_launch_us": round(avg_ms * 1e3, 2), "median_launch_us": round(1e3 * statistics.median(durs), 2),
             "peak_source": src}
 

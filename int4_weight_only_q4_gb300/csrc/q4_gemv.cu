@@ -128,6 +128,26 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// 16-byte asynchronous copy global -> shared (through L2 only) and its group bookkeeping.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// wait_group with a run-time count n in [0, N]
+template <int N>
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+    if constexpr (N == 0) {
+        cp_async_wait<0>();
+    } else {
+        if (n >= N) cp_async_wait<N>();
+        else cp_async_wait_upto<N - 1>(n);
+    }
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
@@ -221,6 +241,14 @@ __device__ __forceinline__ uint2 ld_dep_u2(const void* p) {
     asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p) : "memory");
     return r;
 }
+__device__ __forceinline__ uint4 ld_dep_u4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
 __device__ __forceinline__ float ld_dep_f32(const float* p) {
     float r;
     asm volatile("ld.global.f32 %0, [%1];" : "=f"(r) : "l"(p) : "memory");
@@ -303,6 +331,29 @@ __device__ __forceinline__ void group_dot(const uint4& qa, const uint4& qb, cons
     }
 }
 
+// The tensor-core dot of one group with this lane's activation fragments in registers (xv[i] =
+// fragments (i, 0) and (i, 1)) as two independent mma chains (words 0-1 and 2-3) added at the
+// end: a fixed order, half the dependent-mma latency.
+__device__ __forceinline__ void group_dot_x4(const uint4& qa, const uint4& qb, const uint4 (&xv)[4],
+                                             float (&c)[4]) {
+    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+    const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+    float c2[4] = {0.f, 0.f, 0.f, 0.f};
+    c[0] = c[1] = c[2] = c[3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float (&d)[4] = (i < 2) ? c : c2;
+        const uint32_t wa8 = wa[i] >> 8, wb8 = wb[i] >> 8;
+        mma_bf16_m16n8k16(d, lo_nibbles(wa[i]), lo_nibbles(wb[i]), hi_nibbles(wa[i]), hi_nibbles(wb[i]), xv[i].x,
+                          xv[i].y);
+        mma_bf16_m16n8k16(d, lo_nibbles(wa8), lo_nibbles(wb8), hi_nibbles(wa8), hi_nibbles(wb8), xv[i].z, xv[i].w);
+    }
+    c[0] += c2[0];
+    c[1] += c2[1];
+    c[2] += c2[2];
+    c[3] += c2[3];
+}
+
 // acc += scale * (c * f) + min * S for rows q (scale/min packed in sa_ma) and q+8 (sb_mb);
 // f = 2^(133-a) of batch columns 2t, 2t+1 undoes the staging scale.
 template <bool XG = false>
@@ -343,7 +394,12 @@ __device__ __forceinline__ uint32_t bf16x2_scale(uint32_t v, float m1, float m2)
 // 2p+1, 2p+5}; S[gl][n] = sum over the group (fixed order: 8 sequential adds, then a 16-lane xor
 // tree).  Every thread in [0, nthr) calls this; nthr is a multiple of 32.  colmax: 8 words of
 // scratch shared memory.
-template <int BT, typename Sync>
+// LM (for the prepared copy in global memory): entries (gl, i, 0) and (gl, i, 1) of lane L are one
+// 16-byte word, uint4 (gl * 4 + i) * 4BT + L, so that each of a warp's four loads per group is one
+// contiguous run; and the group sums are stored already divided by fac (S[gl][n] * 2^(a_n-133),
+// an exact power-of-two scaling), so that a consumer applies fac once per output instead of once
+// per group.
+template <int BT, bool LM = false, typename Sync>
 __device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0, int Gs, uint2* xs, float* ssum,
                                         float* fac, unsigned* colmax, int tid, int nthr, Sync sync) {
     const int items = Gs * B * 16;  // (local group, column, chunk t, word i); (t, i) fastest
@@ -411,9 +467,19 @@ __device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0,
         p1.x = bf16x2_scale(p1.x, m1, m2);
         p0.y = bf16x2_scale(p0.y, m1, m2 * 0.0625f);
         p1.y = bf16x2_scale(p1.y, m1, m2 * 0.0625f);
-        const size_t base = xfrag_index<BT>(gl, i, 0) + n * 4 + tt;
-        xs[base] = p0;
-        xs[base + 4 * BT] = p1;
+        if constexpr (LM) {
+            const size_t li = (static_cast<size_t>(gl) * 4 + i) * 4 * BT + n * 4 + tt;
+            reinterpret_cast<uint4*>(xs)[li] = make_uint4(p0.x, p0.y, p1.x, p1.y);
+            if (ti == 0) {  // this thread wrote ssum[gl * 8 + n] in the first pass
+                const int e = a - 133, e1 = e < -63 ? -63 : e, e2 = e - e1;
+                ssum[gl * 8 + n] = (ssum[gl * 8 + n] * __int_as_float((e1 + 127) << 23)) *
+                                   __int_as_float((e2 + 127) << 23);
+            }
+        } else {
+            const size_t base = xfrag_index<BT>(gl, i, 0) + n * 4 + tt;
+            xs[base] = p0;
+            xs[base + 4 * BT] = p1;
+        }
     }
     if (tid < 8) {
         const int e = static_cast<int>(colmax[tid] >> 23) - 127;
@@ -886,9 +952,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) q4_stream_kernel(const __grid
 }
 
 // ================================================================== activation prep + tile kernel
-// q4_xprep_kernel: one CTA per matrix stages its activations once, in global memory, exactly as
-// stage_x does in shared memory for the kernels above: x in B-fragment order scaled per column,
-// the per-group sums of x and the per-column factors.
+// q4_xprep_kernel: one CTA per matrix stages its activations once, in global memory, as stage_x
+// does in shared memory for the kernels above (layout LM): x in B-fragment order scaled per
+// column, the per-group sums of x divided by the column factors, and the column factors.
 struct PrepJob {
     const uint16_t* x;
     uint2* xf;
@@ -910,20 +976,27 @@ __global__ void __launch_bounds__(256) q4_xprep_kernel(const __grid_constant__ P
     grid_dependency_wait();  // x may be the previous kernel's output
     allow_dependents();
     const PrepJob& j = p.j[blockIdx.x];
-    stage_x<BT>(j.x, j.K, p.B, 0, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, 256, [] { __syncthreads(); });
+    stage_x<BT, true>(j.x, j.K, p.B, 0, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, 256,
+                      [] { __syncthreads(); });
 }
 
-// q4_tiles_kernel: one CTA per SM, persistent over a list of independent matrices, no block-wide
-// barrier after the start.  CTA c owns one row block of every matrix (rotated per matrix); its
-// tiles, matrix after matrix, form one list that the warps take from a shared counter.  A warp
-// computes a whole 16-row tile: all K/128 groups in order, codes from the L1 records with DEPTH
-// records in registers and `l2_ahead` more requested from L2, activations from the prepared
-// global copy, the sum kept in registers, Y written by the warp.  Which warp takes which tile
-// does not change any arithmetic.
+// q4_tiles_ring_kernel: one CTA per SM, persistent over a list of independent matrices, no
+// block-wide barrier after the start.  CTA c owns one row block of every matrix (rotated per
+// matrix); its tiles, matrix after matrix, form one list that the warps take from a shared
+// counter.  A warp computes a whole 16-row tile: all K/128 groups in order, the sum in
+// registers, Y written by the warp.  Each warp streams its records through S shared-memory slots
+// with cp.async, S-1 records ahead of the one it computes.  The loading side takes the warp's next
+// tile as soon as the current one is fully requested, so loading runs on across tile and matrix
+// boundaries, and hands the tiles to the computing side through a small per-warp queue.  Exactly
+// one commit group per record step (an empty one once the list is exhausted) keeps the wait count
+// constant: record c sits in slot c % S, and the slot refilled in step c is the one read in step
+// c - 1, whose values are already in registers.  The 64 scale/min bytes are written by lanes 0-3
+// and read by all lanes, which cp.async.wait_group + __syncwarp order.  Which warp takes which
+// tile changes no arithmetic.
 struct TileMat {
     const uint8_t* tiled;
-    const uint2* xf;
-    const float* S;
+    const uint4* xf;  // prepared activations, one 16-byte word per lane and fragment pair
+    const float* S;   // group sums divided by the column factors
     const float* fac;
     float* y;
     int N, K;
@@ -933,19 +1006,24 @@ struct TileMat {
 struct TileParams {
     int n_mats;
     int B;
-    int l2_ahead;
-    int pad;
     TileMat m[kMaxMats];
 };
 
-template <int WARPS, int DEPTH, int BT>
-__global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_kernel(const __grid_constant__ TileParams p) {
-    __shared__ int prefix[kMaxMats + 1];  // this CTA's tiles in matrices [0, i)
-    __shared__ int tfirst[kMaxMats];      // first tile of this CTA's row block in matrix i
+constexpr int kItemQ = 16;  // per-warp queue of tiles requested but not yet computed (> S)
+
+template <int WARPS, int S, int BT>
+__global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __grid_constant__ TileParams p) {
+    static_assert(S >= 2 && S < kItemQ, "ring depth");
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int prefix[kMaxMats + 1];   // this CTA's tiles in matrices [0, i)
+    __shared__ int tfirst[kMaxMats];       // first tile of this CTA's row block in matrix i
     __shared__ int next_item;
+    __shared__ int2 itemq[WARPS][kItemQ];  // (matrix, tile)
     const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int t = lane & 3, q = lane >> 2;
     const int B = p.B;
+    unsigned char* ring = smem + static_cast<size_t>(warp) * S * kRecBytes;
     if (threadIdx.x == 0) {
         int acc = 0;
         for (int i = 0; i < p.n_mats; ++i) {
@@ -966,77 +1044,121 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_kernel(const __grid_co
     }
     __syncthreads();
     const int total = prefix[p.n_mats];
-    bool waited = false;
-    int mi = 0;  // matrix cursor: items only increase, so it only moves forward
-    for (;;) {
-        int item = 0;
-        if (lane == 0) item = atomicAdd(&next_item, 1);
-        item = __shfl_sync(0xffffffffu, item, 0);
-        if (item >= total) break;
-        while (prefix[mi + 1] <= item) ++mi;
+
+    // ---- loading side (warp-uniform state)
+    int scan = 0;  // matrix cursor: items only increase, so it only moves forward
+    const uint8_t* ld_ptr = nullptr;
+    int ld_left = 0;  // records of the current tile not yet requested
+    bool ld_done = false;
+    int nq = 0;  // tiles handed to the computing side
+    int wr = 0;  // byte offset of the slot the next record goes to
+    auto issue = [&]() {
+        if (ld_left == 0 && !ld_done) {
+            int item = 0;
+            if (lane == 0) item = atomicAdd(&next_item, 1);
+            item = __shfl_sync(0xffffffffu, item, 0);
+            if (item < total) {
+                while (prefix[scan + 1] <= item) ++scan;
+                const TileMat& m = p.m[scan];
+                const int G = m.K >> 7;
+                const int tile = tfirst[scan] + (item - prefix[scan]);
+                ld_ptr = m.tiled + static_cast<size_t>(tile) * G * kRecBytes;
+                ld_left = G;
+                if (lane == 0) itemq[warp][nq % kItemQ] = make_int2(scan, tile);
+                ++nq;
+            } else {
+                ld_done = true;
+            }
+        }
+        if (ld_left > 0) {
+            unsigned char* dst = ring + wr;
+            cp_async16(dst + 16 * lane, ld_ptr + 16 * lane);
+            cp_async16(dst + 512 + 16 * lane, ld_ptr + 512 + 16 * lane);
+            if (lane < 4) cp_async16(dst + 1024 + 16 * lane, ld_ptr + 1024 + 16 * lane);
+            ld_ptr += kRecBytes;
+            --ld_left;
+        }
+        cp_async_commit();
+        wr = (wr + kRecBytes == S * kRecBytes) ? 0 : wr + kRecBytes;
+    };
+#pragma unroll 1
+    for (int s = 0; s < S - 1; ++s) issue();  // weights are read-only: before the wait
+
+    grid_dependency_wait();  // the prepared activations come from the kernel before
+    allow_dependents();
+
+    // ---- computing side
+    const bool xon = q < B;
+    int pq = 0;  // tiles taken from the queue
+    int rd = 0;  // byte offset of the slot read next
+    int mi = 0, tile = 0, G = 0, g = 0;
+    const uint4* xq = nullptr;
+    const float* Sg = nullptr;
+    auto take_tile = [&]() {
+        __syncwarp();  // lane 0's queue entry is visible to all lanes
+        const int2 e = itemq[warp][pq % kItemQ];
+        ++pq;
+        mi = e.x;
+        tile = e.y;
         const TileMat& m = p.m[mi];
-        const int G = m.K >> 7;
-        const int tile = tfirst[mi] + (item - prefix[mi]);
-        const uint8_t* rec0 = m.tiled + static_cast<size_t>(tile) * G * kRecBytes;
-        // records DEPTH .. DEPTH + l2_ahead - 1 to L2, the first DEPTH into registers
-        if (lane == 0 && p.l2_ahead > 0 && G > DEPTH)
-            prefetch_l2_bulk(rec0 + DEPTH * kRecBytes, static_cast<uint32_t>(min(p.l2_ahead, G - DEPTH) * kRecBytes));
-        Stage st[DEPTH];
-#pragma unroll
-        for (int d = 0; d < DEPTH; ++d) {
-            const uint8_t* r = rec0 + static_cast<size_t>(min(d, G - 1)) * kRecBytes;
-            st[d].qa = ld_stream_u4(r + 16 * lane);
-            st[d].qb = ld_stream_u4(r + 512 + 16 * lane);
-            const uint2 v = ld_stream_u2(r + 1024 + 8 * q);
-            st[d].sa_ma = v.x;
-            st[d].sb_mb = v.y;
-        }
-        if (!waited) {
-            grid_dependency_wait();  // the prepared activations come from the kernel before
-            allow_dependents();
-            waited = true;
-        }
-        const float f0 = ld_dep_f32(m.fac + 2 * t), f1 = ld_dep_f32(m.fac + 2 * t + 1);
+        G = m.K >> 7;
+        g = 0;
+        xq = m.xf + lane;
+        Sg = m.S + 2 * t;
+    };
+    if (nq > 0) {
+        take_tile();
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        auto step = [&](int gg, Stage& slot) {
-            const Stage cur = slot;
-            // refill with the record DEPTH ahead (the last one again near the end: an L1/L2 hit)
-            const int gn = min(gg + DEPTH, G - 1);
-            const uint8_t* r = rec0 + static_cast<size_t>(gn) * kRecBytes;
-            if (lane == 0 && p.l2_ahead > 0 && gg + DEPTH + p.l2_ahead < G)
-                prefetch_l2_bulk(r + static_cast<size_t>(p.l2_ahead) * kRecBytes, kRecBytes);
-            slot.qa = ld_stream_u4(r + 16 * lane);
-            slot.qb = ld_stream_u4(r + 512 + 16 * lane);
-            const uint2 v = ld_stream_u2(r + 1024 + 8 * q);
-            slot.sa_ma = v.x;
-            slot.sb_mb = v.y;
+#pragma unroll 1
+        for (;;) {
+            cp_async_wait<S - 2>();  // this step's record has landed
+            __syncwarp();
+            uint4 xv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                xv[j] = xon ? ld_dep_u4(xq + (g * 4 + j) * (4 * BT)) : make_uint4(0u, 0u, 0u, 0u);
+            const uint2 sv = ld_dep_u2(Sg + g * 8);
+            const unsigned char* rec = ring + rd;
+            const uint4 qa = lds128(rec + 16 * lane);
+            const uint4 qb = lds128(rec + 512 + 16 * lane);
+            const uint2 sc = lds64(rec + 1024 + 8 * q);
+            rd = (rd + kRecBytes == S * kRecBytes) ? 0 : rd + kRecBytes;
+            issue();  // S - 1 records ahead, into the slot read in the step before
             float cc[4];
-            group_dot<true, BT, true>(cur.qa, cur.qb, m.xf + xfrag_index<BT>(gg, 0, 0), lane, B, cc);
-            group_epilogue<true>(acc, cc, cur.sa_ma, cur.sb_mb, m.S + gg * 8 + 2 * t, f0, f1);
-        };
-        int g = 0;
-        for (; g + DEPTH <= G; g += DEPTH) {
-#pragma unroll
-            for (int d = 0; d < DEPTH; ++d) step(g + d, st[d]);
-        }
-#pragma unroll
-        for (int d = 0; d < DEPTH; ++d)
-            if (g + d < G) step(g + d, st[d]);
-        const int ra = 16 * tile + q, rbw = ra + 8;
-        const int c0 = 2 * t, c1 = 2 * t + 1;
-        if (ra < m.N) {
-            if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + ra] = acc[0];
-            if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + ra] = acc[1];
-        }
-        if (rbw < m.N) {
-            if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + rbw] = acc[2];
-            if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + rbw] = acc[3];
+            group_dot_x4(qa, qb, xv, cc);
+            const float Sx = __uint_as_float(sv.x), Sy = __uint_as_float(sv.y);
+            const float sa = half_bits_to_f32(sc.x), ma = half_bits_to_f32(sc.x >> 16);
+            const float sb = half_bits_to_f32(sc.y), mb = half_bits_to_f32(sc.y >> 16);
+            acc[0] = fmaf(sa, cc[0], acc[0]);
+            acc[0] = fmaf(ma, Sx, acc[0]);
+            acc[1] = fmaf(sa, cc[1], acc[1]);
+            acc[1] = fmaf(ma, Sy, acc[1]);
+            acc[2] = fmaf(sb, cc[2], acc[2]);
+            acc[2] = fmaf(mb, Sx, acc[2]);
+            acc[3] = fmaf(sb, cc[3], acc[3]);
+            acc[3] = fmaf(mb, Sy, acc[3]);
+            if (++g == G) {
+                const TileMat& m = p.m[mi];
+                const float f0 = ld_dep_f32(m.fac + 2 * t), f1 = ld_dep_f32(m.fac + 2 * t + 1);
+                const int ra = 16 * tile + q, rbw = ra + 8;
+                const int c0 = 2 * t, c1 = 2 * t + 1;
+                if (ra < m.N) {
+                    if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + ra] = acc[0] * f0;
+                    if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + ra] = acc[1] * f1;
+                }
+                if (rbw < m.N) {
+                    if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + rbw] = acc[2] * f0;
+                    if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + rbw] = acc[3] * f1;
+                }
+                acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                // the next tile's first record was requested at least one step ago, so the queue
+                // holds it unless the list is exhausted
+                if (pq == nq) break;
+                take_tile();
+            }
         }
     }
-    if (!waited) {
-        grid_dependency_wait();
-        allow_dependents();
-    }
+    cp_async_wait<0>();
 }
 
 // ================================================================== argmax
@@ -1111,6 +1233,7 @@ struct Knobs {
     int ksplit_min;
     bool pdl, rotate;
     int l2_ahead;      // direct kernel on L1: units prefetched into L2 ahead of the loads
+    int tw, ts;        // tile kernel: warps per CTA and cp.async ring slots per warp
 };
 
 Knobs knobs() {
@@ -1131,6 +1254,10 @@ Knobs knobs() {
     k.rotate = env_int("Q4_ROTATE", 1) != 0;
     k.l2_ahead = env_int("Q4_L2_AHEAD", 8);
     if (k.l2_ahead < 0 || k.l2_ahead > 64) k.l2_ahead = 8;
+    // tile kernel shape: warps per CTA, and ring slots per warp that go with it
+    k.tw = env_int("Q4_TW", 24);
+    if (k.tw != 16 && k.tw != 32) k.tw = 24;
+    k.ts = k.tw == 16 ? 8 : k.tw == 24 ? 6 : 4;
     return k;
 }
 
@@ -1427,7 +1554,6 @@ q4_status tiles_stream(const Knobs& k, const q4_matrix* mats, int n, float* cons
         std::memset(&tp, 0, sizeof tp);
         tp.n_mats = cnt;
         tp.B = B;
-        tp.l2_ahead = k.l2_ahead;
         int grid = 1;
         for (int i = 0; i < cnt; ++i) {
             const q4_matrix& W = mats[base + i];
@@ -1436,7 +1562,7 @@ q4_status tiles_stream(const Knobs& k, const q4_matrix* mats, int n, float* cons
             if (independent) off += prep_bytes(W.K, bt);
             TileMat& m = tp.m[i];
             m.tiled = static_cast<const uint8_t*>(W.tiled);
-            m.xf = reinterpret_cast<const uint2*>(w);
+            m.xf = reinterpret_cast<const uint4*>(w);
             m.S = reinterpret_cast<const float*>(w + G * 256 * bt);
             m.fac = m.S + G * 8;
             m.y = Y[base + i];
@@ -1450,13 +1576,18 @@ q4_status tiles_stream(const Knobs& k, const q4_matrix* mats, int n, float* cons
         }
         using TilesFn = void (*)(TileParams);
         TilesFn tf = nullptr;
-        if (k.depth == 2)
-            tf = bt == 1 ? q4_tiles_kernel<16, 2, 1> : bt == 2 ? q4_tiles_kernel<16, 2, 2>
-               : bt == 4 ? q4_tiles_kernel<16, 2, 4> : q4_tiles_kernel<16, 2, 8>;
+        const size_t smem = static_cast<size_t>(k.tw) * k.ts * kRecBytes;
+        if (k.tw == 24)
+            tf = bt == 1 ? q4_tiles_ring_kernel<24, 6, 1> : bt == 2 ? q4_tiles_ring_kernel<24, 6, 2>
+               : bt == 4 ? q4_tiles_ring_kernel<24, 6, 4> : q4_tiles_ring_kernel<24, 6, 8>;
+        else if (k.tw == 16)
+            tf = bt == 1 ? q4_tiles_ring_kernel<16, 8, 1> : bt == 2 ? q4_tiles_ring_kernel<16, 8, 2>
+               : bt == 4 ? q4_tiles_ring_kernel<16, 8, 4> : q4_tiles_ring_kernel<16, 8, 8>;
         else
-            tf = bt == 1 ? q4_tiles_kernel<16, 4, 1> : bt == 2 ? q4_tiles_kernel<16, 4, 2>
-               : bt == 4 ? q4_tiles_kernel<16, 4, 4> : q4_tiles_kernel<16, 4, 8>;
-        const q4_status s = launch(tf, dev, static_cast<unsigned>(grid), 16u * 32u, 0, stream, k.pdl, tp);
+            tf = bt == 1 ? q4_tiles_ring_kernel<32, 4, 1> : bt == 2 ? q4_tiles_ring_kernel<32, 4, 2>
+               : bt == 4 ? q4_tiles_ring_kernel<32, 4, 4> : q4_tiles_ring_kernel<32, 4, 8>;
+        const unsigned threads = static_cast<unsigned>(k.tw * 32);
+        const q4_status s = launch(tf, dev, static_cast<unsigned>(grid), threads, smem, stream, k.pdl, tp);
         if (s != Q4_OK) return s;
     }
     return Q4_OK;

@@ -358,6 +358,30 @@ def test_decode_step_independent_and_chained_agree(q4):
     q4.device_status()
 
 
+@pytest.mark.parametrize("env", [{"Q4_TW": "16"}, {"Q4_TW": "24"}, {"Q4_TW": "32"}])
+def test_tile_kernel_shapes(q4, monkeypatch, env):
+    """Every warp count / ring depth of the tile kernel: oracle parity and batch invariance; the
+    shapes share one arithmetic order, so they agree bit for bit with the default."""
+    mats, xs, ws_np = _decode_mats(q4, 1, 3, base=40)
+    X = [bf16_tensor(x) for x in xs]
+    Y0 = [torch.empty((3, m.N), device="cuda") for m in mats]
+    q4.decode_step(mats, X, Y0)
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    Y = [torch.empty((3, m.N), device="cuda") for m in mats]
+    Y1 = [torch.empty((1, m.N), device="cuda") for m in mats]
+    q4.decode_step(mats, X, Y)
+    q4.decode_step(mats, [x[1:2].contiguous() for x in X], Y1)
+    torch.cuda.synchronize()
+    for i in range(len(mats)):
+        assert torch.equal(Y[i][1], Y1[i][0]), i
+        assert torch.equal(Y[i], Y0[i]), i
+        rows = _sample_rows(ws_np[i].shape[0], n=128, seed=i)
+        assert within_tol(f"tile kernel {env} matrix {i}", Y[i].cpu().numpy()[:, rows],
+                          oracle_rows(ws_np[i], xs[i], rows)), i
+    q4.device_status()
+
+
 def test_long_list_spans_several_launches(q4):
     """More matrices than one launch's table: the list is cut into launches, results unchanged."""
     n = 140
