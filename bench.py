@@ -478,6 +478,39 @@ def end_to_end(q4, torch, g, xs, dev, steps, barrier):
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
 
 
+def run_profile_case(args) -> int:
+    """A small case for ncu: `layers` decode layers + the head with seeded random codes in the tiled
+    layout, activations prepared once, then five step_stream launches and one argmax (no timing)."""
+    import torch
+    import int4_weight_only_q4_gb300 as q4
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed)
+    B = args.profile_batch
+    shapes = [sh for sh in step_shapes()[:3 * args.profile_step]] + [step_shapes()[-1]]
+    mats = []
+    for N, K in shapes:
+        codes = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev, generator=gen)
+        sc = (torch.rand((N, K // 128), device=dev, generator=gen) * 0.01 + 1e-3).half()
+        mn = (torch.rand((N, K // 128), device=dev, generator=gen) * -0.05).half()
+        W = q4.QuantizedMatrix(codes, sc, mn, N, K).build_tiled()
+        W.codes = W.scales = W.mins = None
+        mats.append(W)
+    X = [torch.randn((B, K), device=dev, generator=gen).to(torch.bfloat16) for _, K in shapes]
+    Y = [torch.empty((B, N), device=dev) for N, _ in shapes]
+    ws = q4.Workspace(q4.step_workspace_bytes([K for _, K in shapes], B))
+    q4.step_prepare(mats, X, ws)
+    for _ in range(5):
+        q4.step_stream(mats, Y, B, ws)
+    q4.argmax(Y[-1])
+    torch.cuda.synchronize()
+    q4.device_status()
+    print(json.dumps({"profile_case": f"{args.profile_step} layers + head", "B": B, "matrices": len(shapes),
+                      "algorithmic_bytes_per_stream_launch": sum(algo_bytes(N, K, B) for N, K in shapes)}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -487,7 +520,12 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-step", type=int, default=0,
+                    help="run only a small profiling case of this many layers + the head, then exit")
+    ap.add_argument("--profile-batch", type=int, default=1)
     args = ap.parse_args()
+    if args.profile_step > 0:
+        return run_profile_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -109,6 +109,16 @@ __device__ __forceinline__ void mma_bf16_m16n8k16(float (&d)[4], uint32_t a0, ui
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = A * B (the accumulator input is zero)
+__device__ __forceinline__ void mma_bf16_m16n8k16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                     uint32_t a3, uint32_t b0, uint32_t b1) {
+    const float z = 0.f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
@@ -338,14 +348,17 @@ __device__ __forceinline__ void group_dot_x4(const uint4& qa, const uint4& qb, c
                                              float (&c)[4]) {
     const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
     const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
-    float c2[4] = {0.f, 0.f, 0.f, 0.f};
-    c[0] = c[1] = c[2] = c[3] = 0.f;
+    float c2[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         float (&d)[4] = (i < 2) ? c : c2;
         const uint32_t wa8 = wa[i] >> 8, wb8 = wb[i] >> 8;
-        mma_bf16_m16n8k16(d, lo_nibbles(wa[i]), lo_nibbles(wb[i]), hi_nibbles(wa[i]), hi_nibbles(wb[i]), xv[i].x,
-                          xv[i].y);
+        if (i == 0 || i == 2)
+            mma_bf16_m16n8k16_zc(d, lo_nibbles(wa[i]), lo_nibbles(wb[i]), hi_nibbles(wa[i]), hi_nibbles(wb[i]),
+                                 xv[i].x, xv[i].y);
+        else
+            mma_bf16_m16n8k16(d, lo_nibbles(wa[i]), lo_nibbles(wb[i]), hi_nibbles(wa[i]), hi_nibbles(wb[i]),
+                              xv[i].x, xv[i].y);
         mma_bf16_m16n8k16(d, lo_nibbles(wa8), lo_nibbles(wb8), hi_nibbles(wa8), hi_nibbles(wb8), xv[i].z, xv[i].w);
     }
     c[0] += c2[0];
@@ -1051,8 +1064,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
     int ld_left = 0;  // records of the current tile not yet requested
     bool ld_done = false;
     int nq = 0;  // tiles handed to the computing side
-    int wr = 0;  // byte offset of the slot the next record goes to
-    auto issue = [&]() {
+    // record r goes to the slot at byte offset (r % S) * kRecBytes
+    auto issue = [&](int slot_off) {
         if (ld_left == 0 && !ld_done) {
             int item = 0;
             if (lane == 0) item = atomicAdd(&next_item, 1);
@@ -1062,7 +1075,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
                 const TileMat& m = p.m[scan];
                 const int G = m.K >> 7;
                 const int tile = tfirst[scan] + (item - prefix[scan]);
-                ld_ptr = m.tiled + static_cast<size_t>(tile) * G * kRecBytes;
+                ld_ptr = m.tiled + static_cast<size_t>(tile) * G * kRecBytes + 16 * lane;
                 ld_left = G;
                 if (lane == 0) itemq[warp][nq % kItemQ] = make_int2(scan, tile);
                 ++nq;
@@ -1071,29 +1084,29 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
             }
         }
         if (ld_left > 0) {
-            unsigned char* dst = ring + wr;
-            cp_async16(dst + 16 * lane, ld_ptr + 16 * lane);
-            cp_async16(dst + 512 + 16 * lane, ld_ptr + 512 + 16 * lane);
-            if (lane < 4) cp_async16(dst + 1024 + 16 * lane, ld_ptr + 1024 + 16 * lane);
+            unsigned char* dst = ring + slot_off + 16 * lane;
+            cp_async16(dst, ld_ptr);
+            cp_async16(dst + 512, ld_ptr + 512);
+            if (lane < 4) cp_async16(dst + 1024, ld_ptr + 1024);
             ld_ptr += kRecBytes;
             --ld_left;
         }
         cp_async_commit();
-        wr = (wr + kRecBytes == S * kRecBytes) ? 0 : wr + kRecBytes;
     };
-#pragma unroll 1
-    for (int s = 0; s < S - 1; ++s) issue();  // weights are read-only: before the wait
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) issue(s * kRecBytes);  // weights are read-only: before the wait
 
     grid_dependency_wait();  // the prepared activations come from the kernel before
     allow_dependents();
 
     // ---- computing side
-    const bool xon = q < B;
+    // Lanes whose batch column is >= B read column 0's activations: the mma keeps batch columns
+    // apart, and those outputs are never stored.
+    const int xlane = q < B ? lane : t;
     int pq = 0;  // tiles taken from the queue
-    int rd = 0;  // byte offset of the slot read next
     int mi = 0, tile = 0, G = 0, g = 0;
-    const uint4* xq = nullptr;
-    const float* Sg = nullptr;
+    const uint4* xg = nullptr;  // this group's activation words for this lane
+    const float* Sg = nullptr;  // this group's sums for columns 2t, 2t+1
     auto take_tile = [&]() {
         __syncwarp();  // lane 0's queue entry is visible to all lanes
         const int2 e = itemq[warp][pq % kItemQ];
@@ -1103,59 +1116,66 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
         const TileMat& m = p.m[mi];
         G = m.K >> 7;
         g = 0;
-        xq = m.xf + lane;
+        xg = m.xf + xlane;
         Sg = m.S + 2 * t;
+    };
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int rd = 0;                    // slot of this step's record
+    int prev = (S - 1) * kRecBytes;  // slot read in the step before (the first step's is unused)
+    // one record step; false once the warp's list is done
+    auto step = [&]() -> bool {
+        cp_async_wait<S - 2>();  // this step's record has landed
+        __syncwarp();
+        uint4 xv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) xv[j] = ld_dep_u4(xg + j * (4 * BT));
+        const uint2 sv = ld_dep_u2(Sg);
+        const unsigned char* rec = ring + rd;
+        const uint4 qa = lds128(rec + 16 * lane);
+        const uint4 qb = lds128(rec + 512 + 16 * lane);
+        const uint2 sc = lds64(rec + 1024 + 8 * q);
+        issue(prev);  // S - 1 records ahead, into the slot read one step ago
+        prev = rd;
+        rd = rd + kRecBytes == S * kRecBytes ? 0 : rd + kRecBytes;
+        float cc[4];
+        group_dot_x4(qa, qb, xv, cc);
+        const float Sx = __uint_as_float(sv.x), Sy = __uint_as_float(sv.y);
+        const float sa = half_bits_to_f32(sc.x), ma = half_bits_to_f32(sc.x >> 16);
+        const float sb = half_bits_to_f32(sc.y), mb = half_bits_to_f32(sc.y >> 16);
+        acc[0] = fmaf(sa, cc[0], acc[0]);
+        acc[0] = fmaf(ma, Sx, acc[0]);
+        acc[1] = fmaf(sa, cc[1], acc[1]);
+        acc[1] = fmaf(ma, Sy, acc[1]);
+        acc[2] = fmaf(sb, cc[2], acc[2]);
+        acc[2] = fmaf(mb, Sx, acc[2]);
+        acc[3] = fmaf(sb, cc[3], acc[3]);
+        acc[3] = fmaf(mb, Sy, acc[3]);
+        xg += 16 * BT;
+        Sg += 8;
+        if (++g < G) return true;
+        const TileMat& m = p.m[mi];
+        const float f0 = ld_dep_f32(m.fac + 2 * t), f1 = ld_dep_f32(m.fac + 2 * t + 1);
+        const int ra = 16 * tile + q, rbw = ra + 8;
+        const int c0 = 2 * t, c1 = 2 * t + 1;
+        if (ra < m.N) {
+            if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + ra] = acc[0] * f0;
+            if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + ra] = acc[1] * f1;
+        }
+        if (rbw < m.N) {
+            if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + rbw] = acc[2] * f0;
+            if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + rbw] = acc[3] * f1;
+        }
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        // the next tile's first record was requested at least one step ago, so the queue holds it
+        // unless the list is exhausted
+        if (pq == nq) return false;
+        take_tile();
+        return true;
     };
     if (nq > 0) {
         take_tile();
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-        for (;;) {
-            cp_async_wait<S - 2>();  // this step's record has landed
-            __syncwarp();
-            uint4 xv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                xv[j] = xon ? ld_dep_u4(xq + (g * 4 + j) * (4 * BT)) : make_uint4(0u, 0u, 0u, 0u);
-            const uint2 sv = ld_dep_u2(Sg + g * 8);
-            const unsigned char* rec = ring + rd;
-            const uint4 qa = lds128(rec + 16 * lane);
-            const uint4 qb = lds128(rec + 512 + 16 * lane);
-            const uint2 sc = lds64(rec + 1024 + 8 * q);
-            rd = (rd + kRecBytes == S * kRecBytes) ? 0 : rd + kRecBytes;
-            issue();  // S - 1 records ahead, into the slot read in the step before
-            float cc[4];
-            group_dot_x4(qa, qb, xv, cc);
-            const float Sx = __uint_as_float(sv.x), Sy = __uint_as_float(sv.y);
-            const float sa = half_bits_to_f32(sc.x), ma = half_bits_to_f32(sc.x >> 16);
-            const float sb = half_bits_to_f32(sc.y), mb = half_bits_to_f32(sc.y >> 16);
-            acc[0] = fmaf(sa, cc[0], acc[0]);
-            acc[0] = fmaf(ma, Sx, acc[0]);
-            acc[1] = fmaf(sa, cc[1], acc[1]);
-            acc[1] = fmaf(ma, Sy, acc[1]);
-            acc[2] = fmaf(sb, cc[2], acc[2]);
-            acc[2] = fmaf(mb, Sx, acc[2]);
-            acc[3] = fmaf(sb, cc[3], acc[3]);
-            acc[3] = fmaf(mb, Sy, acc[3]);
-            if (++g == G) {
-                const TileMat& m = p.m[mi];
-                const float f0 = ld_dep_f32(m.fac + 2 * t), f1 = ld_dep_f32(m.fac + 2 * t + 1);
-                const int ra = 16 * tile + q, rbw = ra + 8;
-                const int c0 = 2 * t, c1 = 2 * t + 1;
-                if (ra < m.N) {
-                    if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + ra] = acc[0] * f0;
-                    if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + ra] = acc[1] * f1;
-                }
-                if (rbw < m.N) {
-                    if (c0 < B) m.y[static_cast<size_t>(c0) * m.N + rbw] = acc[2] * f0;
-                    if (c1 < B) m.y[static_cast<size_t>(c1) * m.N + rbw] = acc[3] * f1;
-                }
-                acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-                // the next tile's first record was requested at least one step ago, so the queue
-                // holds it unless the list is exhausted
-                if (pq == nq) break;
-                take_tile();
-            }
+        while (step()) {
         }
     }
     cp_async_wait<0>();
@@ -1168,14 +1188,53 @@ __device__ __forceinline__ bool ranks_above(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
+__device__ __forceinline__ float4 ld_dep_f4(const float4* p) {
+    float4 r;
+    asm volatile("ld.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
+
+// One CTA per row.  The row is read as 16-byte words, four independent loads in flight per
+// thread (a scalar head up to the first 16-byte boundary and a scalar tail); ranks_above is a
+// total order, so the visiting order does not change the result.
 __global__ void __launch_bounds__(1024) q4_argmax_kernel(const float* __restrict__ Y, int N, int32_t* idx) {
     grid_dependency_wait();  // Y is usually the previous kernel's output
     const float* row = Y + static_cast<size_t>(blockIdx.x) * N;
     float bv = -__int_as_float(0x7f800000);
     int bi = 0x7fffffff;
-    for (int i = threadIdx.x; i < N; i += blockDim.x) {
-        const float v = ld_dep_f32(row + i);
+    auto consider = [&](float v, int i) {
         if (ranks_above(v, i, bv, bi)) { bv = v; bi = i; }
+    };
+    const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(row) & 15u) >> 2);  // row is 4-byte aligned
+    const int head = min(N, (4 - mis) & 3);
+    const int n4 = (N - head) >> 2;
+    const int tail0 = head + 4 * n4;
+    const int tid = static_cast<int>(threadIdx.x);
+    if (tid < head) consider(ld_dep_f32(row + tid), tid);
+    if (tail0 + tid < N) consider(ld_dep_f32(row + tail0 + tid), tail0 + tid);
+    const float4* row4 = reinterpret_cast<const float4*>(row + head);
+    constexpr int kU = 4;
+    for (int base = tid; base < n4; base += kU * 1024) {
+        float4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int j = base + u * 1024;
+            v[u] = j < n4 ? ld_dep_f4(row4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int j = base + u * 1024;
+            if (j < n4) {
+                const int i = head + 4 * j;
+                consider(v[u].x, i);
+                consider(v[u].y, i + 1);
+                consider(v[u].z, i + 2);
+                consider(v[u].w, i + 3);
+            }
+        }
     }
     for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -1255,8 +1314,8 @@ Knobs knobs() {
     k.l2_ahead = env_int("Q4_L2_AHEAD", 8);
     if (k.l2_ahead < 0 || k.l2_ahead > 64) k.l2_ahead = 8;
     // tile kernel shape: warps per CTA, and ring slots per warp that go with it
-    k.tw = env_int("Q4_TW", 24);
-    if (k.tw != 16 && k.tw != 32) k.tw = 24;
+    k.tw = env_int("Q4_TW", 32);
+    if (k.tw != 16 && k.tw != 24) k.tw = 32;
     k.ts = k.tw == 16 ? 8 : k.tw == 24 ? 6 : 4;
     return k;
 }

@@ -290,6 +290,16 @@ def test_argmax_ties_nan_and_layout(q4):
     got = q4.argmax(Y).cpu().numpy()
     assert got.tolist() == np.argmax(y, axis=1).tolist()
     assert got[0] == 5 and got[1] == 0 and got[2] == 123 and got[3] == 70000 and got[4] == 17
+    # short and oddly aligned rows: scalar head, vector body and scalar tail of every size
+    rng = np.random.default_rng(1)
+    for N in (1, 2, 3, 4, 5, 7, 9, 4097, 4099):
+        y = rng.standard_normal((8, N)).astype(np.float32)
+        got = q4.argmax(torch.from_numpy(y).cuda()).cpu().numpy()
+        assert got.tolist() == np.argmax(y, axis=1).tolist(), N
+        flat = torch.from_numpy(rng.standard_normal(3 * N + 1).astype(np.float32)).cuda()
+        view = flat[1:].view(3, N)                 # rows start 4 bytes past a 16-byte boundary
+        got = q4.argmax(view).cpu().numpy()
+        assert got.tolist() == np.argmax(view.cpu().numpy(), axis=1).tolist(), N
 
 
 # ----------------------------------------------------------------------------- decode step
