@@ -10,7 +10,9 @@ import os
 import re
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libq4.so")
+# Q4_LIBRARY_PATH selects another build of the same library (e.g. to compare two builds side by
+# side); by default the in-tree build next to this file.
+LIB_PATH = os.environ.get("Q4_LIBRARY_PATH") or os.path.join(HERE, "libq4.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "q4.h")
 
 if not os.path.exists(LIB_PATH):

@@ -60,6 +60,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "q4.h"
 
@@ -986,8 +987,10 @@ struct PrepParams {
 template <int BT>
 __global__ void __launch_bounds__(256) q4_xprep_kernel(const __grid_constant__ PrepParams p) {
     __shared__ unsigned colmax[8];
-    grid_dependency_wait();  // x may be the previous kernel's output
+    // The tile kernel after this one may start at once: it streams weights (read-only) until its
+    // own wait, which returns only when this grid is complete.
     allow_dependents();
+    grid_dependency_wait();  // x may be the previous kernel's output
     const PrepJob& j = p.j[blockIdx.x];
     stage_x<BT, true>(j.x, j.K, p.B, 0, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, 256,
                       [] { __syncthreads(); });
@@ -1181,6 +1184,216 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
     cp_async_wait<0>();
 }
 
+// q4_flat_kernel: one matrix per launch, the work split evenly over every warp of the grid.  In the
+// tiled layout a matrix is one run of records, tile after tile (G = K/128 records a tile).  CTA c
+// takes a contiguous range of whole tiles (the ranges differ by at most one tile), and its WARPS
+// warps split the range's records evenly: with R = WARPS u + e records, warp w takes u + 1
+// records if w < e, else u, in warp order.  So each warp's share is one contiguous byte range,
+// which lane 0 asks L2 for at once (up to kFlatPf records, then kFlatPf ahead of the loads),
+// streamed through S shared-memory slots with cp.async as in q4_tiles_ring_kernel.  A warp's
+// records split at tile boundaries into segments.  A segment that covers a whole tile writes Y
+// directly; the others (at most the first and the last of a warp) leave their partial sums in
+// shared memory (slot 0 for the first, slot 1 for the last) and count themselves in the ticket of
+// the tile's first warp; the warp that completes the count adds the partials in warp (= record)
+// order and writes Y.  Nothing is shared between CTAs and nothing outlives the launch.
+// XS: the CTA stages the activations itself (stage_x, layout LM) into shared memory after its
+// grid-dependency wait, while its first weight records are already on the way; otherwise they
+// come prepared from q4_xprep_kernel in global memory.
+// The split depends on N, K and the SM count only, so each batch column is computed in the same
+// order for every B.
+constexpr int kFlatPf = 16;
+
+struct FlatParams {
+    const uint8_t* tiled;
+    const uint16_t* x;  // XS: the activations
+    const uint4* xf;    // otherwise: prepared activations (layout LM) ...
+    const float* S;     // ... group sums divided by the column factors
+    const float* fac;   // ... column factors
+    float* y;
+    int N, K, B;
+    int T;  // tiles
+};
+
+template <int WARPS, int S, int BT, bool XS>
+__global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_constant__ FlatParams p) {
+    static_assert(S >= 2, "ring depth");
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int ticket[WARPS];
+    __shared__ unsigned colmax[8];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int t = lane & 3, q = lane >> 2;
+    const int B = p.B;
+    const int G = p.K >> 7;
+    unsigned char* ring = smem + static_cast<size_t>(warp) * S * kRecBytes;
+    float4* part = reinterpret_cast<float4*>(smem + static_cast<size_t>(WARPS) * S * kRecBytes);  // [WARPS][2][32]
+    unsigned char* xsm = reinterpret_cast<unsigned char*>(part + WARPS * 2 * 32);
+    if (threadIdx.x < WARPS) ticket[threadIdx.x] = 0;
+
+    // this CTA's tiles and this warp's records (local record index within the CTA's range)
+    const int nb = static_cast<int>(gridDim.x);
+    const int tu = p.T / nb, te = p.T % nb;
+    const int c = static_cast<int>(blockIdx.x);
+    const int t0 = c * tu + (c < te ? c : te);
+    const int Rc = (tu + (c < te ? 1 : 0)) * G;
+    const int u = Rc / WARPS, e = Rc % WARPS;
+    auto run_start = [&](int v) { return v * u + (v < e ? v : e); };
+    auto owner = [&](int r) { return r < e * (u + 1) ? r / (u + 1) : e + (r - e * (u + 1)) / u; };
+    const int r0 = run_start(warp);
+    const int n = u + (warp < e ? 1 : 0);
+
+    // ---- loading side
+    const uint8_t* ld_ptr = p.tiled + (static_cast<size_t>(t0) * G + r0) * kRecBytes + 16 * lane;
+    int ld_left = n;
+    if (lane == 0 && n > 0) prefetch_l2_bulk(ld_ptr, static_cast<uint32_t>(min(n, kFlatPf) * kRecBytes));
+    auto issue = [&](int slot_off) {
+        if (ld_left > 0) {
+            if (lane == 0 && ld_left > kFlatPf)
+                prefetch_l2_bulk(ld_ptr + static_cast<size_t>(kFlatPf) * kRecBytes, kRecBytes);
+            unsigned char* dst = ring + slot_off + 16 * lane;
+            cp_async16(dst, ld_ptr);
+            cp_async16(dst + 512, ld_ptr + 512);
+            if (lane < 4) cp_async16(dst + 1024, ld_ptr + 1024);
+            ld_ptr += kRecBytes;
+            --ld_left;
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) issue(s * kRecBytes);  // weights are read-only: before the wait
+
+    grid_dependency_wait();  // x (or its prepared copy) comes from the kernel before
+    allow_dependents();
+
+    const uint4* xf;
+    const float* Sb;
+    const float* fac;
+    if constexpr (XS) {
+        uint2* xs = reinterpret_cast<uint2*>(xsm);
+        float* ssum = reinterpret_cast<float*>(xsm + static_cast<size_t>(G) * 256 * BT);
+        float* fs = ssum + G * 8;
+        stage_x<BT, true>(p.x, p.K, B, 0, G, xs, ssum, fs, colmax, static_cast<int>(threadIdx.x), WARPS * 32,
+                          [] { __syncthreads(); });
+        __syncthreads();
+        xf = reinterpret_cast<const uint4*>(xs);
+        Sb = ssum;
+        fac = fs;
+    } else {
+        __syncthreads();  // the tickets
+        xf = p.xf;
+        Sb = p.S;
+        fac = p.fac;
+    }
+    auto ldx4 = [&](const uint4* a) -> uint4 {
+        if constexpr (XS) return *a;
+        else return ld_dep_u4(a);
+    };
+    auto ldx2 = [&](const float* a) -> uint2 {
+        if constexpr (XS) return *reinterpret_cast<const uint2*>(a);
+        else return ld_dep_u2(a);
+    };
+    auto ldf = [&](const float* a) -> float {
+        if constexpr (XS) return *a;
+        else return ld_dep_f32(a);
+    };
+
+    // ---- computing side
+    const int xlane = q < B ? lane : t;  // columns >= B read column 0: their outputs are dropped
+    const float f0 = ldf(fac + 2 * t), f1 = ldf(fac + 2 * t + 1);
+    const int c0 = 2 * t, c1 = 2 * t + 1;
+    int tile = r0 / G;  // local tile
+    int g = r0 - tile * G;
+    int gs = g;  // first group of the current segment
+    bool first_seg = true;
+    const uint4* xg = xf + xlane + g * (16 * BT);
+    const float* Sg = Sb + 2 * t + g * 8;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int rd = 0, prev = (S - 1) * kRecBytes;
+
+    auto store_y = [&](const float (&a)[4]) {
+        const int ra = 16 * (t0 + tile) + q, rbw = ra + 8;
+        if (ra < p.N) {
+            if (c0 < B) p.y[static_cast<size_t>(c0) * p.N + ra] = a[0] * f0;
+            if (c1 < B) p.y[static_cast<size_t>(c1) * p.N + ra] = a[1] * f1;
+        }
+        if (rbw < p.N) {
+            if (c0 < B) p.y[static_cast<size_t>(c0) * p.N + rbw] = a[2] * f0;
+            if (c1 < B) p.y[static_cast<size_t>(c1) * p.N + rbw] = a[3] * f1;
+        }
+    };
+    auto flush = [&](int ge) {  // segment [gs, ge) of `tile` is complete
+        if (gs == 0 && ge == G) {
+            store_y(acc);
+            return;
+        }
+        part[(warp * 2 + (first_seg ? 0 : 1)) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __threadfence_block();
+        __syncwarp();
+        const int tb = tile * G;
+        const int wf = owner(tb), wl = owner(tb + G - 1);  // the warps sharing this tile
+        int tk = 0;
+        if (lane == 0) tk = atomicAdd(&ticket[wf], 1);
+        tk = __shfl_sync(0xffffffffu, tk, 0);
+        if (tk != wl - wf) return;
+        __threadfence_block();  // every partial of the tile is visible
+        // warp wf's segment is its last one (slot 1) when its run began in an earlier tile; every
+        // other segment opens its warp's run (slot 0)
+        const volatile float4* pp = part + (wf * 2 + (run_start(wf) < tb ? 1 : 0)) * 32 + lane;
+        float s[4] = {pp->x, pp->y, pp->z, pp->w};
+        for (int v = wf + 1; v <= wl; ++v) {
+            pp = part + (v * 2) * 32 + lane;
+            s[0] += pp->x;
+            s[1] += pp->y;
+            s[2] += pp->z;
+            s[3] += pp->w;
+        }
+        store_y(s);
+    };
+
+#pragma unroll 1
+    for (int i = 0; i < n; ++i) {
+        cp_async_wait<S - 2>();  // this step's record has landed
+        __syncwarp();
+        uint4 xv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) xv[j] = ldx4(xg + j * (4 * BT));
+        const uint2 sv = ldx2(Sg);
+        const unsigned char* rec = ring + rd;
+        const uint4 qa = lds128(rec + 16 * lane);
+        const uint4 qb = lds128(rec + 512 + 16 * lane);
+        const uint2 sc = lds64(rec + 1024 + 8 * q);
+        issue(prev);  // S - 1 records ahead, into the slot read one step ago
+        prev = rd;
+        rd = rd + kRecBytes == S * kRecBytes ? 0 : rd + kRecBytes;
+        float cc[4];
+        group_dot_x4(qa, qb, xv, cc);
+        const float Sx = __uint_as_float(sv.x), Sy = __uint_as_float(sv.y);
+        const float sa = half_bits_to_f32(sc.x), ma = half_bits_to_f32(sc.x >> 16);
+        const float sb = half_bits_to_f32(sc.y), mb = half_bits_to_f32(sc.y >> 16);
+        acc[0] = fmaf(sa, cc[0], acc[0]);
+        acc[0] = fmaf(ma, Sx, acc[0]);
+        acc[1] = fmaf(sa, cc[1], acc[1]);
+        acc[1] = fmaf(ma, Sy, acc[1]);
+        acc[2] = fmaf(sb, cc[2], acc[2]);
+        acc[2] = fmaf(mb, Sx, acc[2]);
+        acc[3] = fmaf(sb, cc[3], acc[3]);
+        acc[3] = fmaf(mb, Sy, acc[3]);
+        xg += 16 * BT;
+        Sg += 8;
+        ++g;
+        if (g == G || i == n - 1) {
+            flush(g);
+            first_seg = false;
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            ++tile;
+            g = gs = 0;
+            xg = xf + xlane;
+            Sg = Sb + 2 * t;
+        }
+    }
+    cp_async_wait<0>();
+}
+
 // ================================================================== argmax
 __device__ __forceinline__ bool ranks_above(float v, int i, float bv, int bi) {
     const bool vn = v != v, bn = bv != bv;
@@ -1298,7 +1511,7 @@ struct Knobs {
 Knobs knobs() {
     Knobs k{};
     k.kernel = env_int("Q4_KERNEL", -1);  // -1: chosen per call
-    if (k.kernel < -1 || k.kernel > 5) k.kernel = -1;
+    if (k.kernel < -1 || k.kernel > 6) k.kernel = -1;
     k.warps = env_int("Q4_WARPS", 16);
     k.depth = env_int("Q4_DEPTH", 4);
     const bool ok = (k.warps == 16 && (k.depth == 2 || k.depth == 4 || k.depth == 6)) ||
@@ -1320,15 +1533,45 @@ Knobs knobs() {
     return k;
 }
 
-bool uses_l1(int kernel) { return kernel == 0 || kernel == 3 || kernel == 4 || kernel == 5; }
+bool uses_l1(int kernel) { return kernel == 0 || kernel == 3 || kernel == 4 || kernel == 5 || kernel == 6; }
 bool is_stream(int kernel) { return kernel == 3; }
 bool is_tiles(int kernel) { return kernel == 5; }
+bool is_flat(int kernel) { return kernel == 6; }
 
 // Workspace of the tile kernel: the prepared activations of one matrix (x fragments, group
 // sums, column factors), for batch tile bt.
 size_t prep_bytes(int64_t K, int bt) {
     const size_t G = static_cast<size_t>(K / 128);
     return align256(G * 256 * bt + G * 32 + 32);
+}
+
+// Flat kernel: warps per CTA, ring slots, CTAs (one per SM, at most one per tile), shared memory
+// and workspace.
+constexpr int kFlatSlots = 4;
+int flat_grid(int64_t N, int sms) {
+    const int64_t T = (N + 15) / 16;
+    return static_cast<int>(T < sms ? T : sms);
+}
+// shared memory of a flat launch of fw warps; XS adds the staged activations
+size_t flat_smem(int fw, int64_t K, int bt, bool xs) {
+    return static_cast<size_t>(fw) * kFlatSlots * kRecBytes + static_cast<size_t>(fw) * 2 * 32 * 16 +
+           (xs ? prep_bytes(K, bt) : 0);
+}
+// Warps per CTA: 32 where the activations of 8 batch columns fit beside the 32 rings, else 16.
+// A function of K only (it fixes the split, hence the arithmetic order), never of B.
+int flat_warps(int64_t K) { return flat_smem(32, K, 8, true) <= kSmemLimit ? 32 : 16; }
+bool flat_xs(int64_t K, int bt) { return flat_smem(flat_warps(K), K, bt, true) <= kSmemLimit; }
+// Workspace of a list on the flat kernel: the prepared activations when they do not fit in shared
+// memory, a slice per matrix (independent) or one shared slice.
+size_t flat_list_bytes(const int64_t* N, const int64_t* K, int n, int bt, bool independent) {
+    (void)N;
+    size_t sum = 0, one_max = 0;
+    for (int i = 0; i < n; ++i) {
+        const size_t one = flat_xs(K[i], bt) ? 0 : align256(prep_bytes(K[i], bt));
+        sum += one;
+        if (one > one_max) one_max = one;
+    }
+    return independent ? sum : one_max;
 }
 
 // The split of one (N, K) matrix.  Depends on N, K, the SM count and the kernel -- never on B.
@@ -1348,7 +1591,7 @@ bool default_shape(const Knobs& k) { return k.warps == 16 && k.depth == 4; }
 // non-default direct shapes (instantiated for 8 columns only).
 int batch_tile(const Knobs& k, int kernel, int B) {
     const int bt = B <= 1 ? 1 : (B <= 2 ? 2 : (B <= 4 ? 4 : 8));
-    if (kernel == 5) return bt;
+    if (kernel == 5 || kernel == 6) return bt;
     if (is_stream(kernel)) return (k.sw == 8 && k.sd == 2) ? bt : 8;
     return default_shape(k) ? bt : 8;
 }
@@ -1367,7 +1610,7 @@ bool make_plan(int64_t N, int64_t K, int sms, const Knobs& k, int kernel, Plan* 
     Plan p{};
     const int G = static_cast<int>(K / 128);
     const int64_t T_all = (N + 15) / 16;
-    if (is_tiles(kernel)) {
+    if (is_tiles(kernel) || is_flat(kernel)) {
         p.row_blocks = static_cast<int>(T_all < sms ? T_all : sms);
         p.k_splits = 1;
         p.gs_max = G;
@@ -1422,6 +1665,7 @@ size_t plan_ws_bytes(const Plan& p, int64_t N, int B) {
 
 size_t job_ws_bytes(const Knobs& k, int kernel, const Plan& p, int64_t N, int64_t K, int B) {
     if (is_tiles(kernel)) return prep_bytes(K, batch_tile(k, kernel, B));
+    if (is_flat(kernel)) return flat_list_bytes(&N, &K, 1, batch_tile(k, kernel, B), true);
     return align256(plan_ws_bytes(p, N, B));
 }
 
@@ -1546,15 +1790,21 @@ unsigned block_threads(const Knobs& k, int kernel) {
 // The default: a list of independent matrices runs as one persistent tile-kernel launch (no
 // barrier between matrices); a single matrix, or a list whose launches must follow one another,
 // runs the direct kernel on the tiled copy, which splits K across the warps of a CTA.
-int default_kernel(int n, bool independent) { return (independent && n > 1) ? 5 : 0; }
+// Independent lists of several matrices: the tile kernel.  One matrix at a time: the flat kernel
+// when the matrix has fewer than two 16-row tiles per SM (its split keeps every warp busy), else
+// the direct kernel.  A function of the shapes and the SM count only, never of B.
+int default_kernel(int n, bool independent, int64_t N = 0, int sms = 0) {
+    if (independent && n > 1) return 5;
+    return (sms > 0 && (N + 15) / 16 < 2 * static_cast<int64_t>(sms)) ? 6 : 0;
+}
 
-q4_status effective_kernel(const Knobs& k, const q4_matrix* mats, int n, bool independent, int* kernel) {
+q4_status effective_kernel(const Knobs& k, const q4_matrix* mats, int n, bool independent, int sms, int* kernel) {
     bool all_l1 = true, all_l0 = true;
     for (int i = 0; i < n; ++i) {
         all_l1 = all_l1 && mats[i].tiled != nullptr;
         all_l0 = all_l0 && has_l0(mats[i]);
     }
-    int kn = k.kernel >= 0 ? k.kernel : default_kernel(n, independent);
+    int kn = k.kernel >= 0 ? k.kernel : default_kernel(n, independent, mats[0].N, sms);
     if (uses_l1(kn) && !all_l1) kn = (kn == 4) ? 2 : 1;
     if (!uses_l1(kn) && !all_l0) kn = (kn == 2) ? 4 : 0;
     if (uses_l1(kn) ? !all_l1 : !all_l0) return Q4_ERR_INVALID_ARG;
@@ -1652,6 +1902,56 @@ q4_status tiles_stream(const Knobs& k, const q4_matrix* mats, int n, float* cons
     return Q4_OK;
 }
 
+// Each matrix of a list on the flat kernel, one launch per matrix (after an activation prep launch
+// when the activations do not fit in shared memory), stream-ordered.  An independent list gives
+// every matrix its own workspace slice, a chained one reuses one slice.
+q4_status flat_run(const Knobs& k, const q4_matrix* mats, int n, const uint16_t* const* X, float* const* Y, int B,
+                   void* ws, bool independent, int dev, int sms, cudaStream_t stream) {
+    const int bt = batch_tile(k, 6, B);
+    unsigned char* base = static_cast<unsigned char*>(ws);
+    for (int i = 0; i < n; ++i) {
+        const q4_matrix& W = mats[i];
+        const bool xs = flat_xs(W.K, bt);
+        const size_t G = static_cast<size_t>(W.K / 128);
+        FlatParams fp;
+        std::memset(&fp, 0, sizeof fp);
+        fp.tiled = static_cast<const uint8_t*>(W.tiled);
+        fp.x = X[i];
+        fp.y = Y[i];
+        fp.N = static_cast<int>(W.N);
+        fp.K = static_cast<int>(W.K);
+        fp.B = B;
+        fp.T = static_cast<int>((W.N + 15) / 16);
+        if (!xs) {
+            q4_status s = tiles_prepare(k, &W, 1, &X[i], B, base, true, dev, stream);
+            if (s != Q4_OK) return s;
+            fp.xf = reinterpret_cast<const uint4*>(base);
+            fp.S = reinterpret_cast<const float*>(base + G * 256 * bt);
+            fp.fac = fp.S + G * 8;
+            if (independent) base += align256(prep_bytes(W.K, bt));
+        }
+        using FlatFn = void (*)(FlatParams);
+        const int fw = flat_warps(W.K);
+        FlatFn ff;
+        if (fw == 32 && xs)
+            ff = bt == 1 ? q4_flat_kernel<32, kFlatSlots, 1, true> : bt == 2 ? q4_flat_kernel<32, kFlatSlots, 2, true>
+               : bt == 4 ? q4_flat_kernel<32, kFlatSlots, 4, true> : q4_flat_kernel<32, kFlatSlots, 8, true>;
+        else if (fw == 32)
+            ff = bt == 1 ? q4_flat_kernel<32, kFlatSlots, 1, false> : bt == 2 ? q4_flat_kernel<32, kFlatSlots, 2, false>
+               : bt == 4 ? q4_flat_kernel<32, kFlatSlots, 4, false> : q4_flat_kernel<32, kFlatSlots, 8, false>;
+        else if (xs)
+            ff = bt == 1 ? q4_flat_kernel<16, kFlatSlots, 1, true> : bt == 2 ? q4_flat_kernel<16, kFlatSlots, 2, true>
+               : bt == 4 ? q4_flat_kernel<16, kFlatSlots, 4, true> : q4_flat_kernel<16, kFlatSlots, 8, true>;
+        else
+            ff = bt == 1 ? q4_flat_kernel<16, kFlatSlots, 1, false> : bt == 2 ? q4_flat_kernel<16, kFlatSlots, 2, false>
+               : bt == 4 ? q4_flat_kernel<16, kFlatSlots, 4, false> : q4_flat_kernel<16, kFlatSlots, 8, false>;
+        const q4_status s = launch(ff, dev, static_cast<unsigned>(flat_grid(W.N, sms)), static_cast<unsigned>(fw * 32),
+                                   flat_smem(fw, W.K, bt, xs), stream, k.pdl, fp);
+        if (s != Q4_OK) return s;
+    }
+    return Q4_OK;
+}
+
 size_t step_prep_bytes(const int64_t* K, int n, int B) {
     const Knobs k = knobs();
     const int bt = batch_tile(k, 5, B);
@@ -1672,12 +1972,21 @@ q4_status run(const q4_matrix* mats, int n, const uint16_t* const* X, float* con
         if ((s = check_io(X[i], B, Y[i])) != Q4_OK) return s;
     }
     const Knobs k = knobs();
-    int kernel = 0;
-    q4_status st = effective_kernel(k, mats, n, independent, &kernel);
-    if (st != Q4_OK) return st;
     int dev = 0;
     const int sms = device_sm_count(&dev);
     if (sms <= 0) return Q4_ERR_CUDA;
+    if (!independent && n > 1 && k.kernel < 0) {
+        // a chained list runs one matrix per launch anyway: each with its own kernel choice, all in
+        // the one workspace slice (stream order keeps them apart)
+        for (int i = 0; i < n; ++i) {
+            const q4_status s = run(&mats[i], 1, &X[i], &Y[i], B, ws, ws_bytes, true, stream);
+            if (s != Q4_OK) return s;
+        }
+        return Q4_OK;
+    }
+    int kernel = 0;
+    q4_status st = effective_kernel(k, mats, n, independent, sms, &kernel);
+    if (st != Q4_OK) return st;
     // plans and workspace: a persistent list gives every k-split matrix its own slice
     size_t need = 0;
     for (int i = 0; i < n; ++i) {
@@ -1686,11 +1995,17 @@ q4_status run(const q4_matrix* mats, int n, const uint16_t* const* X, float* con
         const size_t b = job_ws_bytes(k, kernel, pl, mats[i].N, mats[i].K, B);
         need = independent ? need + b : (b > need ? b : need);
     }
+    if (is_flat(kernel)) {
+        std::vector<int64_t> Ns(n), Ks(n);
+        for (int i = 0; i < n; ++i) { Ns[i] = mats[i].N; Ks[i] = mats[i].K; }
+        need = flat_list_bytes(Ns.data(), Ks.data(), n, batch_tile(k, kernel, B), independent);
+    }
     if (need > 0) {
         if (!ws || ws_bytes < need) return Q4_ERR_WORKSPACE;
         if (!aligned(ws, 16)) return Q4_ERR_MISALIGNED;
     }
     const int per_launch = independent ? kMaxMats : 1;
+    if (is_flat(kernel)) return flat_run(k, mats, n, X, Y, B, ws, independent, dev, sms, stream);
     if (is_tiles(kernel)) {
         q4_status s2 = tiles_prepare(k, mats, n, X, B, ws, independent, dev, stream);
         if (s2 != Q4_OK) return s2;
@@ -1751,14 +2066,29 @@ size_t workspace_for(const int64_t* N, const int64_t* K, int n, int B, bool inde
     const int sms = device_sm_count(nullptr);
     if (sms <= 0) return 0;
     const Knobs k = knobs();
-    const int kernel = k.kernel >= 0 ? k.kernel : default_kernel(n, independent);
+    if (!independent && n > 1 && k.kernel < 0) {  // one matrix at a time (see run)
+        size_t m = 0;
+        for (int i = 0; i < n; ++i) {
+            const size_t b = workspace_for(&N[i], &K[i], 1, B, true);
+            if (check_shape(N[i], K[i]) != Q4_OK) return 0;
+            m = b > m ? b : m;
+        }
+        return m;
+    }
+    const int kernel = k.kernel >= 0 ? k.kernel : default_kernel(n, independent, N[0], sms);
+    // the flat kernel falls back to kernel 1 for matrices without a tiled copy: cover both
+    const int kernel2 = is_flat(kernel) ? 1 : kernel;
     size_t need = 0;
     for (int i = 0; i < n; ++i) {
         if (check_shape(N[i], K[i]) != Q4_OK) return 0;
         Plan p;
-        if (!make_plan(N[i], K[i], sms, k, kernel, &p)) return 0;
-        const size_t b = job_ws_bytes(k, kernel, p, N[i], K[i], B);
+        if (!make_plan(N[i], K[i], sms, k, kernel2, &p)) return 0;
+        const size_t b = job_ws_bytes(k, kernel2, p, N[i], K[i], B);
         need = independent ? need + b : (b > need ? b : need);
+    }
+    if (is_flat(kernel)) {
+        const size_t f = flat_list_bytes(N, K, n, batch_tile(k, kernel, B), independent);
+        if (f > need) need = f;
     }
     return need;
 }
@@ -1804,12 +2134,14 @@ extern "C" q4_status q4_plan(int64_t N, int64_t K, q4_plan_info* out) {
     const int sms = device_sm_count(nullptr);
     if (sms <= 0) return Q4_ERR_CUDA;
     Knobs k = knobs();
-    if (k.kernel < 0) k.kernel = default_kernel(1, true);
+    if (k.kernel < 0) k.kernel = default_kernel(1, true, N, sms);
     Plan p;
     if (!make_plan(N, K, sms, k, k.kernel, &p)) return Q4_ERR_UNSUPPORTED_SHAPE;
     out->row_blocks = p.row_blocks;
     out->k_splits = p.k_splits;
-    out->warps_per_cta = is_tiles(k.kernel) ? 16 : static_cast<int32_t>(block_threads(k, k.kernel) / 32);
+    out->warps_per_cta = is_tiles(k.kernel)  ? k.tw
+                         : is_flat(k.kernel) ? flat_warps(K)
+                                             : static_cast<int32_t>(block_threads(k, k.kernel) / 32);
     out->prefetch_depth = is_stream(k.kernel) ? k.sw * k.sd : k.depth;
     out->kernel = k.kernel;
     out->sm_count = sms;

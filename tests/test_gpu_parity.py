@@ -210,14 +210,17 @@ def test_k_split_path_parity_and_invariance(q4, monkeypatch, kernel):
     assert int(ws.buf[:256].view(torch.int32)[: q4.plan(N, K)["row_blocks"]].abs().sum()) == 0
 
 
-@pytest.mark.parametrize("env", [{"Q4_KERNEL": "1"}, {"Q4_KERNEL": "2"}, {"Q4_KERNEL": "3"}, {"Q4_KERNEL": "4"},
+@pytest.mark.parametrize("env", [{"Q4_KERNEL": "0"}, {"Q4_KERNEL": "1"}, {"Q4_KERNEL": "2"}, {"Q4_KERNEL": "3"},
+                                 {"Q4_KERNEL": "4"}, {"Q4_KERNEL": "6"}, {"Q4_KERNEL": "6", "Q4_PDL": "0"},
                                  {"Q4_KERNEL": "3", "Q4_SW": "8", "Q4_SD": "1"},
                                  {"Q4_KERNEL": "3", "Q4_SW": "4", "Q4_SD": "4"},
                                  {"Q4_KERNEL": "3", "Q4_SW": "6", "Q4_SD": "2"},
                                  {"Q4_KERNEL": "3", "Q4_KSPLIT": "3"},
-                                 {"Q4_DEPTH": "2"}, {"Q4_DEPTH": "6"}, {"Q4_WARPS": "8", "Q4_DEPTH": "4"},
-                                 {"Q4_WARPS": "8", "Q4_DEPTH": "8"}, {"Q4_KERNEL": "1", "Q4_DEPTH": "6"},
-                                 {"Q4_PDL": "0"}, {"Q4_KSPLIT": "2"}, {"Q4_ROTATE": "0"}])
+                                 {"Q4_KERNEL": "0", "Q4_DEPTH": "2"}, {"Q4_KERNEL": "0", "Q4_DEPTH": "6"},
+                                 {"Q4_KERNEL": "0", "Q4_WARPS": "8", "Q4_DEPTH": "4"},
+                                 {"Q4_KERNEL": "0", "Q4_WARPS": "8", "Q4_DEPTH": "8"},
+                                 {"Q4_KERNEL": "1", "Q4_DEPTH": "6"},
+                                 {"Q4_PDL": "0"}, {"Q4_KERNEL": "0", "Q4_KSPLIT": "2"}, {"Q4_ROTATE": "0"}])
 def test_kernel_variants(q4, monkeypatch, env):
     for k, v in env.items():
         monkeypatch.setenv(k, v)
@@ -392,6 +395,26 @@ def test_tile_kernel_shapes(q4, monkeypatch, env):
     q4.device_status()
 
 
+def test_single_calls_share_one_workspace(q4):
+    """Single calls on matrices of different shapes, one workspace reused in both orders: every call
+    matches the oracle and repeats bit for bit (nothing a call leaves behind changes the next)."""
+    shapes = [(25088, 3072), (3072, 8192), (100, 1152), (3072, 3072), (4099, 1024), (16, 128)]
+    B = 3
+    probs = [synthetic.random_shape_problem(N, K, B, seed=20 + i) for i, (N, K) in enumerate(shapes)]
+    mats = [q4.QuantizedMatrix.from_float(w) for w, _ in probs]
+    Xs = [bf16_tensor(x) for _, x in probs]
+    ws = q4.Workspace(max(q4.workspace_bytes(N, K, B) for N, K in shapes))
+    first = [q4.gemm_skinny(W, X, workspace=ws) for W, X in zip(mats, Xs)]
+    again = [q4.gemm_skinny(W, X, workspace=ws) for W, X in reversed(list(zip(mats, Xs)))][::-1]
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(first, again)):
+        assert torch.equal(a, b), shapes[i]
+        rows = _sample_rows(shapes[i][0], n=256, seed=i)
+        assert within_tol(f"shared workspace {shapes[i]}", a.cpu().numpy()[:, rows],
+                          oracle_rows(probs[i][0], probs[i][1], rows)), shapes[i]
+    q4.device_status()
+
+
 def test_long_list_spans_several_launches(q4):
     """More matrices than one launch's table: the list is cut into launches, results unchanged."""
     n = 140
@@ -450,7 +473,8 @@ def test_error_statuses_on_device(q4, monkeypatch):
     L = _lib.lib
     # misaligned x
     assert L.q4_gemv(ctypes.byref(m), X.data_ptr() + 2, Y.data_ptr(), None, 0, None) == _lib.Q4_ERR_MISALIGNED
-    # workspace required but missing / too small under a forced k-split
+    # workspace required but missing / too small under a forced k-split of the direct kernel
+    monkeypatch.setenv("Q4_KERNEL", "0")
     monkeypatch.setenv("Q4_KSPLIT", "2")
     need = q4.workspace_bytes(3072, 3072, 1)
     assert need > 0
@@ -460,6 +484,7 @@ def test_error_statuses_on_device(q4, monkeypatch):
         _lib.Q4_ERR_WORKSPACE
     assert L.q4_gemv(ctypes.byref(m), X.data_ptr(), Y.data_ptr(), ws.data_ptr(), need, None) == _lib.Q4_OK
     monkeypatch.delenv("Q4_KSPLIT")
+    monkeypatch.delenv("Q4_KERNEL")
     # a simulated launch failure is reported, and nothing is launched
     Y.fill_(7.0)
     wsz = q4.workspace_bytes(3072, 3072, 1)
