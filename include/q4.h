@@ -88,7 +88,10 @@ typedef struct {
                                 3 stream (bulk copies into a shared-memory ring) on the tiled copy
                                   + tensor-core dot, 4 direct on the tiled copy + CUDA-core fp32 dot,
                                 5 tile kernel: prepared activations + whole 16-row tiles per warp,
-                                  persistent over a list (independent lists of several matrices) */
+                                  persistent over a list (independent lists of several matrices),
+                                6 flat kernel: one matrix, its records split evenly over all warps,
+                                  partials of cut tiles added in shared memory (single matrices
+                                  with fewer than two 16-row tiles per SM) */
     int32_t sm_count;
 } q4_plan_info;
 
@@ -124,8 +127,9 @@ q4_status q4_tile(const q4_matrix* W, void* tiled, size_t tiled_bytes, void* str
 
 /*
  * q4_workspace_bytes -- device workspace a q4_gemv / q4_gemm_skinny call on
- * (N, K, B) needs on the current device (0 when the plan does not split K).
- * The workspace holds fp32 partial sums and arrival counters.  It must be
+ * (N, K, B) needs on the current device (0 when the call needs none).  The
+ * workspace holds fp32 partial sums and arrival counters of a K split, or
+ * the prepared activations when they do not fit in shared memory.  It must be
  * zero-filled once before its first use; every call leaves its counters at
  * zero again when it completes, so the same buffer can be reused by later
  * calls on the same stream (and by graph replays) without clearing.
