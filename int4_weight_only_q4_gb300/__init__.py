@@ -255,7 +255,9 @@ class DecodeStepGraph:
     """One decode step (all matrices, in order) captured once into a CUDA graph and replayed.
 
     The activations and outputs are fixed device buffers: write new activations
-    into ``self.X[i]`` and read ``self.Y[i]`` after ``replay()``.
+    into ``self.X[i]`` and read ``self.Y[i]`` after ``replay()``.  Unless X is
+    given, the activations are views of one contiguous buffer ``self.X_flat``
+    (matrix after matrix, [B, K] each), so a step's inputs arrive in one copy.
     """
 
     def __init__(self, mats, B: int, X=None, Y=None, workspace: Workspace | None = None, device="cuda",
@@ -263,8 +265,13 @@ class DecodeStepGraph:
         self.mats = list(mats)
         self.B = B
         self.independent = independent
-        self.X = X if X is not None else [torch.zeros((B, m.K), dtype=torch.bfloat16, device=device)
-                                           for m in self.mats]
+        if X is None:
+            sizes = [B * m.K for m in self.mats]     # multiples of 128 elements: views stay 16-byte aligned
+            self.X_flat = torch.zeros((sum(sizes),), dtype=torch.bfloat16, device=device)
+            self.X = [v.view(B, m.K) for v, m in zip(torch.split(self.X_flat, sizes), self.mats)]
+        else:
+            self.X_flat = None
+            self.X = X
         self.Y = Y if Y is not None else [torch.empty((B, m.N), dtype=torch.float32, device=device)
                                            for m in self.mats]
         self.ws = workspace if workspace is not None else \
@@ -289,13 +296,17 @@ class DecodeStepGraph:
     def replay(self):
         self.graph.replay()
 
-    def run_host(self, X_host, Y_host, idx_host=None):
-        """One step end to end: copy activations from (pinned) host tensors, replay, copy the
-        outputs (and the argmax indices) back, and wait for them."""
-        for d, h in zip(self.X, X_host):
-            d.copy_(h, non_blocking=True)
+    def run_host(self, X_host, Y_host=None, idx_host=None):
+        """One step end to end: copy the activations from (pinned) host memory -- one tensor laid
+        out like ``X_flat``, or one tensor per matrix -- replay, copy the outputs and/or the argmax
+        indices back, and wait for them."""
+        if isinstance(X_host, torch.Tensor):
+            self.X_flat.copy_(X_host, non_blocking=True)
+        else:
+            for d, h in zip(self.X, X_host):
+                d.copy_(h, non_blocking=True)
         self.graph.replay()
-        for d, h in zip(self.Y, Y_host):
+        for d, h in zip(self.Y, Y_host or []):
             h.copy_(d, non_blocking=True)
         if idx_host is not None and self.idx is not None:
             idx_host.copy_(self.idx, non_blocking=True)

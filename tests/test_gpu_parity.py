@@ -345,6 +345,27 @@ def test_decode_step_graph_equals_eager_and_oracle(q4, B):
         assert within_tol(f"decode step B={B} matrix {i}", y[:, rows], oracle_rows(ws_np[i], xs[i], rows)), i
 
 
+def test_graph_run_host_one_copy(q4):
+    """The activation buffers are views of one contiguous buffer: one pinned host tensor laid out
+    like it feeds the whole step, with the same outputs and argmax as filling the views."""
+    mats, xs, _ = _decode_mats(q4, 1, 2, base=60)
+    g = q4.DecodeStepGraph(mats, 2, with_argmax_of=0)
+    assert all(x.data_ptr() % 16 == 0 for x in g.X)
+    for i, x in enumerate(xs):
+        g.X[i].copy_(bf16_tensor(x))
+    g.replay()
+    Y_ref = [y.clone() for y in g.Y]
+    idx_ref = g.idx.clone()
+    host = g.X_flat.cpu().pin_memory()
+    g.X_flat.zero_()
+    hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in g.Y]
+    hidx = torch.empty(g.idx.shape, dtype=g.idx.dtype).pin_memory()
+    g.run_host(host, hy, hidx)
+    for a, b in zip(hy, Y_ref):
+        assert torch.equal(a, b.cpu())
+    assert torch.equal(hidx, idx_ref.cpu())
+
+
 def test_decode_step_independent_and_chained_agree(q4):
     """Independent lists run the tile kernel, chained ones the direct kernel: both match the oracle,
     agree to fp32 rounding, and each is batch-invariant."""
