@@ -373,6 +373,8 @@ def run_ours(args):
     # the fused 25,088x3072 projection: single calls, and sustained over the step's 36 copies
     fused_single = fused_single_call(q4, torch, mats[0], dev, args)
     fused_sus = fused_sustained(q4, torch, mats, dev, args)
+    # the int8 output head with the argmax fused in
+    head8 = int8_head(q4, torch, dev, args)
 
     # end to end through the public API with pinned host buffers
     e2e = end_to_end(q4, torch, g1, xs1, dev, max(10, args.steps // 20), barrier)
@@ -388,6 +390,7 @@ def run_ours(args):
         "decode_step_us": dec_us, "decode_step_chained_launches_us": chained_us, "step_with_head_us": {"b1": round(ms1 * 1e3, 2), "b8": round(ms8 * 1e3, 2)},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "roofline": roof, "fused_projection_sustained": fused_sus, "fused_gemv_single_call": fused_single,
+        "int8_head_65536x3072": head8,
         "gen_seconds": round(gen_s, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -499,6 +502,54 @@ def fused_sustained(q4, torch, mats, dev, args):
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "us_per_projection": round(avg_ms * 1e3 / len(fused), 3), "avg_launch_us": round(avg_ms * 1e3, 2),
             "algorithmic_bytes_per_launch": byts, "peak_source": src}
+
+
+def int8_head(q4, torch, dev, args):
+    """The int8 output head (65,536 x 3072, per-row fp16 scales) with its argmax fused into the same
+    launch: 8 calls on 8 rotating copies in one CUDA graph, microseconds per call, B=1 and B=8,
+    logits + argmax and argmax only."""
+    N, K, _ = synthetic.SHAPES["head"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 555)
+    heads = []
+    for i in range(8):  # seeded random codes and scales on the device (timing only)
+        codes = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev, generator=gen)
+        sc = (torch.rand((N,), device=dev, generator=gen) * 1e-3 + 1e-4).half()
+        heads.append(q4.Int8Head.from_device(codes, sc))
+    out = {}
+    for B in (1, 8):
+        X = torch.randn((B, K), device=dev).to(torch.bfloat16)
+        Y = torch.empty((B, N), device=dev)
+        idx = torch.empty((B,), dtype=torch.int32, device=dev)
+        ws = heads[0].workspace(B, dev)
+        for logits in (True, False):
+            side = torch.cuda.Stream(device=dev)
+            with torch.cuda.stream(side):
+                for H in heads:
+                    H(X, Y, idx, logits=logits, workspace=ws, stream=side)
+                side.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    for H in heads:
+                        H(X, Y, idx, logits=logits, workspace=ws, stream=side)
+            for _ in range(5):
+                g.replay()
+            n = max(20, args.steps // 40)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = 1e3 * e0.elapsed_time(e1) / (n * len(heads))
+            byts = N * K + 2 * N + 2 * B * K + (4 * B * N if logits else 0) + 4 * B
+            out[f"b{B}_{'logits_argmax' if logits else 'argmax_only'}"] = {
+                "us_per_call": round(us, 3), "GB/s": round(byts / (us * 1e-6) / 1e9, 1)}
+    peak, src = measured_peak_gbs()
+    out["frac_b1_argmax_only"] = round(out["b1_argmax_only"]["GB/s"] / peak, 4)
+    out["kernel"] = "q4_flat_kernel<16, 4, BT, true, true> + q8_argmax_final (8 calls per CUDA graph)"
+    return out
 
 
 def end_to_end(q4, torch, g, xs, dev, steps, barrier):

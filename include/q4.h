@@ -282,6 +282,59 @@ size_t q4_noalloc_scratch_bytes(void);
  */
 q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream);
 
+/* ------------------------------------------------------------------------
+ * The int8 output head.  The rumik-oss-1 write-up keeps every projection in
+ * int4 except the output head ("Steps 9-10: streaming to the speaker": the
+ * audio head moved to int8 with its own CUDA kernel because int4 was
+ * measurably too lossy there; "Step 2": int8 weights as torchao quantized
+ * tensors).  Format (torchao's int8 weight-only scheme; the pages give no more
+ * detail): per output row n an fp16 scale s_n = fp16(max_k |w[n,k]| / 127),
+ * codes c = clamp(rint(w / s_n), -127, 127) as int8, w_hat = c * s_n.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    const int8_t*   codes;   /* [N, K] row-major (device for q8_tile), or NULL once tiled */
+    const uint16_t* scales;  /* [N] fp16 bits, device */
+    int64_t N;
+    int64_t K;               /* K % 128 == 0 */
+    const void*     tiled;   /* q8_tiled_bytes(N, K) bytes, 16-byte aligned, or NULL */
+} q8_matrix;
+
+/* q8_pack_host -- quantise fp32 w [N, K] (host) into codes int8 [N, K] and
+ * scales uint16 [N] (host), as above.  Q4_ERR_INVALID_ARG for null pointers,
+ * non-finite weights or a row whose scale overflows fp16. */
+q4_status q8_pack_host(const float* w, int64_t N, int64_t K, int8_t* codes, uint16_t* scales, int n_threads);
+
+/* q8_tiled_bytes -- bytes of the tiled copy: one 2,048-byte record per 16-row
+ * tile and 128-column group at (tile * K/128 + group) * 2048; lane l's 32 code
+ * bytes of row 16 tile + l/4 (columns 32 (l%4) ..) at 32 l, the same of row
+ * + 8 at 1024 + 32 l; rows >= N are zero.  0 for invalid shapes. */
+size_t q8_tiled_bytes(int64_t N, int64_t K);
+
+/* q8_tile -- build the tiled copy from W->codes on `stream`.  Q4_ERR_INVALID_ARG
+ * for null codes/tiled, Q4_ERR_WORKSPACE if tiled_bytes is too small. */
+q4_status q8_tile(const q8_matrix* W, void* tiled, size_t tiled_bytes, void* stream);
+
+/* q8_head_workspace_bytes -- device workspace of q8_head on (N, K, B): the
+ * per-CTA argmax candidates, and the prepared activations when they do not fit
+ * in shared memory.  No initial content needed.  0 for invalid shapes. */
+size_t q8_head_workspace_bytes(int64_t N, int64_t K, int B);
+
+/*
+ * q8_head -- Y[b, :] = W_hat X[b, :] (fp32 accumulation) for b < B, 1 <= B <= 8,
+ * and/or idx[b] = the index of the largest Y[b, n] (lowest index among equal
+ * maxima, NaN first), computed in the same launch as the logits: each CTA keeps
+ * its best row per column, and a one-CTA pass picks the best of those.
+ *   W    host pointer; W->tiled and W->scales device memory.
+ *   X    device bf16 bits [B, K], 16-byte aligned.
+ *   Y    device fp32 [B, N] (4-byte aligned), or NULL to skip the logits.
+ *   idx  device int32 [B], or NULL to skip the argmax (not both NULL).
+ *   ws   device workspace of ws_bytes >= q8_head_workspace_bytes(N, K, B).
+ * Every batch column is bit-identical to the same call at B = 1 (the split of
+ * the work depends on N, K and the SM count only).  Asynchronous on `stream`.
+ */
+q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float* Y, int32_t* idx, void* ws,
+                  size_t ws_bytes, void* stream);
+
 /*
  * q4_device_status -- wait for `stream`, then read and clear the device error
  * word.  Every wait inside the kernels is bounded; one that gives up sets the

@@ -18,7 +18,7 @@ import numpy as np
 import torch
 
 from ._lib import (Q4_OK, Q4_STEP_INDEPENDENT, Q4Error, check, c_i64, c_vp, header_functions,  # noqa: F401
-                   lib, q4_matrix, q4_plan_info)
+                   lib, q4_matrix, q4_plan_info, q8_matrix)
 
 GROUP = 128
 MAX_B = 8
@@ -26,7 +26,7 @@ MAX_B = 8
 __all__ = ["GROUP", "MAX_B", "Q4Error", "QuantizedMatrix", "Workspace", "pack_host", "plan",
            "workspace_bytes", "decode_step_workspace_bytes", "tiled_bytes", "gemv", "gemm_skinny", "decode_step",
            "argmax", "device_status", "DecodeStepGraph", "step_workspace_bytes", "step_prepare", "step_stream",
-           "gemm_skinny_noalloc",
+           "gemm_skinny_noalloc", "pack_int8_host", "Int8Head",
            "header_functions", "lib"]
 
 
@@ -55,6 +55,18 @@ def pack_host(w: np.ndarray, n_threads: int = 0):
                           int(n_threads))
     check(st, "q4_pack_host")
     return codes, scales, mins
+
+
+def pack_int8_host(w: np.ndarray, n_threads: int = 0):
+    """fp32 [N, K] -> (codes int8 [N, K], scales uint16 [N]) for the int8 output head
+    (q8_pack_host: one symmetric fp16 scale per row)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    codes = np.empty((N, K), np.int8)
+    scales = np.empty((N,), np.uint16)
+    check(lib.q8_pack_host(w.ctypes.data, N, K, codes.ctypes.data, scales.ctypes.data, int(n_threads)),
+          "q8_pack_host")
+    return codes, scales
 
 
 def plan(N: int, K: int) -> dict:
@@ -249,6 +261,63 @@ def argmax(Y: torch.Tensor, idx: torch.Tensor | None = None, stream=None) -> tor
         idx = torch.empty((B,), dtype=torch.int32, device=Y.device)
     check(lib.q4_argmax_f32(_ptr(Y2), B, N, _ptr(idx), _stream_ptr(stream)), "q4_argmax_f32")
     return idx
+
+
+class Int8Head:
+    """An int8 output head resident on the GPU (per-row fp16 scales, tiled copy of the codes):
+    logits and/or their argmax per batch row in one call (q8_head)."""
+
+    def __init__(self, codes: torch.Tensor | None, scales: torch.Tensor, N: int, K: int, tiled: torch.Tensor):
+        self.codes, self.scales, self.N, self.K, self.tiled = codes, scales, N, K, tiled
+
+    @classmethod
+    def from_device(cls, codes: torch.Tensor, scales: torch.Tensor, keep_codes: bool = False, stream=None):
+        """From device codes (int8 [N, K]) and scales (float16 [N], the fp16 bit patterns): builds the
+        tiled copy (q8_tile)."""
+        N, K = codes.shape
+        nb = int(lib.q8_tiled_bytes(N, K))
+        tiled = torch.empty(nb, dtype=torch.uint8, device=codes.device)
+        H = cls(codes, scales, N, K, tiled)
+        check(lib.q8_tile(ctypes.byref(H.c_struct()), _ptr(tiled), nb, _stream_ptr(stream)), "q8_tile")
+        if not keep_codes:
+            torch.cuda.current_stream(codes.device).synchronize()
+            H.codes = None
+        return H
+
+    @classmethod
+    def from_packed(cls, codes: np.ndarray, scales: np.ndarray, device="cuda", keep_codes: bool = False,
+                    stream=None):
+        c = torch.from_numpy(np.ascontiguousarray(codes)).to(device)
+        s = torch.from_numpy(np.ascontiguousarray(scales).view(np.float16)).to(device)
+        return cls.from_device(c, s, keep_codes, stream)
+
+    @classmethod
+    def from_float(cls, w: np.ndarray, device="cuda", n_threads: int = 0, keep_codes: bool = False):
+        return cls.from_packed(*pack_int8_host(w, n_threads), device=device, keep_codes=keep_codes)
+
+    def c_struct(self) -> q8_matrix:
+        p = lambda t: _ptr(t) if t is not None else None
+        return q8_matrix(p(self.codes), p(self.scales), self.N, self.K, p(self.tiled))
+
+    def workspace(self, B: int, device="cuda") -> Workspace:
+        return Workspace(int(lib.q8_head_workspace_bytes(self.N, self.K, B)), device)
+
+    def __call__(self, X: torch.Tensor, Y: torch.Tensor | None = None, idx: torch.Tensor | None = None,
+                 logits: bool = True, argmax: bool = True, workspace: Workspace | None = None, stream=None):
+        """Returns (Y or None, idx or None) for X bf16 [B, K]."""
+        X = _as_bf16(X)
+        B = 1 if X.dim() == 1 else X.shape[0]
+        if logits and Y is None:
+            Y = torch.empty((B, self.N), dtype=torch.float32, device=X.device)
+        if argmax and idx is None:
+            idx = torch.empty((B,), dtype=torch.int32, device=X.device)
+        if workspace is None:
+            workspace = self.workspace(B, X.device)
+        ws_p, ws_n = _ws_args(workspace)
+        m = self.c_struct()
+        check(lib.q8_head(ctypes.byref(m), _ptr(X), B, _ptr(Y) if logits else None, _ptr(idx) if argmax else None,
+                          ws_p, ws_n, _stream_ptr(stream)), "q8_head")
+        return (Y if logits else None), (idx if argmax else None)
 
 
 class DecodeStepGraph:

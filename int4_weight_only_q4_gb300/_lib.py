@@ -29,6 +29,10 @@ class q4_matrix(ctypes.Structure):
     _fields_ = [("codes", c_vp), ("scales", c_vp), ("mins", c_vp), ("N", c_i64), ("K", c_i64), ("tiled", c_vp)]
 
 
+class q8_matrix(ctypes.Structure):
+    _fields_ = [("codes", c_vp), ("scales", c_vp), ("N", c_i64), ("K", c_i64), ("tiled", c_vp)]
+
+
 class q4_plan_info(ctypes.Structure):
     _fields_ = [("row_blocks", ctypes.c_int32), ("k_splits", ctypes.c_int32),
                 ("warps_per_cta", ctypes.c_int32), ("prefetch_depth", ctypes.c_int32),
@@ -82,6 +86,16 @@ lib.q4_device_status.argtypes = [c_vp]
 lib.q4_device_status.restype = ctypes.c_int
 lib.q4_argmax_f32.argtypes = [c_vp, ctypes.c_int, c_i64, c_vp, c_vp]
 lib.q4_argmax_f32.restype = ctypes.c_int
+lib.q8_pack_host.argtypes = [c_vp, c_i64, c_i64, c_vp, c_vp, ctypes.c_int]
+lib.q8_pack_host.restype = ctypes.c_int
+lib.q8_tiled_bytes.argtypes = [c_i64, c_i64]
+lib.q8_tiled_bytes.restype = ctypes.c_size_t
+lib.q8_tile.argtypes = [ctypes.POINTER(q8_matrix), c_vp, ctypes.c_size_t, c_vp]
+lib.q8_tile.restype = ctypes.c_int
+lib.q8_head_workspace_bytes.argtypes = [c_i64, c_i64, ctypes.c_int]
+lib.q8_head_workspace_bytes.restype = ctypes.c_size_t
+lib.q8_head.argtypes = [ctypes.POINTER(q8_matrix), c_vp, ctypes.c_int, c_vp, c_vp, c_vp, ctypes.c_size_t, c_vp]
+lib.q8_head.restype = ctypes.c_int
 lib.q4_status_string.argtypes = [ctypes.c_int]
 lib.q4_status_string.restype = ctypes.c_char_p
 
@@ -102,4 +116,4 @@ def header_functions() -> list[str]:
     """Names of every function declared in include/q4.h."""
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(q4_[a-z0-9_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(q[48]_[a-z0-9_]+)\s*\(", src)))

@@ -72,6 +72,7 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 220 * 1024;  // dynamic; leaves room for static smem under the 227 KB cap
 
 constexpr int kRecBytes = 1088;                 // one L1 record: 16 rows x 128 columns + scale/min
+constexpr int kRec8Bytes = 2048;  // int8 head record: 16 rows x 128 codes
 constexpr int kKC = 8;                          // groups (records) per streamed chunk
 constexpr int kStageBytes = kKC * kRecBytes;    // one stream-ring stage
 constexpr int kMaxMats = 128;                   // matrices per stream launch (kernel parameter table)
@@ -400,6 +401,11 @@ __device__ __forceinline__ uint32_t bf16x2_scale(uint32_t v, float m1, float m2)
     return r;
 }
 
+// A block-wide barrier as a callable (stage_x takes the barrier of its caller).
+struct SyncThreads {
+    __device__ void operator()() const { __syncthreads(); }
+};
+
 // Stage x[:, 128*g0 .. 128*(g0+Gs)) in B-fragment order, the per-group sums of x and the
 // per-column factors.  Column n gets a_n = 120 - e_n (e_n = exponent of the largest |x| of the
 // column's slice, a_n in [6, 253]): entries pairing with low nibbles hold x * 2^a_n, with high
@@ -413,7 +419,10 @@ __device__ __forceinline__ uint32_t bf16x2_scale(uint32_t v, float m1, float m2)
 // contiguous run; and the group sums are stored already divided by fac (S[gl][n] * 2^(a_n-133),
 // an exact power-of-two scaling), so that a consumer applies fac once per output instead of once
 // per group.
-template <int BT, bool LM = false, typename Sync>
+// X8 (with LM, for the int8 head): the k pairing of the int8 operands instead -- word i of lane
+// (n, t) holds mma 2i and 2i+1, each as (x[k], x[k+2]) | (x[k+1], x[k+3]) with k = 32t + 4m for
+// mma m -- and no high-nibble factor.
+template <int BT, bool LM = false, typename Sync, bool X8 = false>
 __device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0, int Gs, uint2* xs, float* ssum,
                                         float* fac, unsigned* colmax, int tid, int nthr, Sync sync) {
     const int items = Gs * B * 16;  // (local group, column, chunk t, word i); (t, i) fastest
@@ -473,14 +482,21 @@ __device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0,
         const float m1 = __int_as_float((a1 + 127) << 23);
         const float m2 = __int_as_float((a - a1 + 127) << 23);
         uint2 p0, p1;
-        p0.x = __byte_perm(v.x, v.z, 0x5410);
-        p0.y = __byte_perm(v.x, v.z, 0x7632);
-        p1.x = __byte_perm(v.y, v.w, 0x5410);
-        p1.y = __byte_perm(v.y, v.w, 0x7632);
-        p0.x = bf16x2_scale(p0.x, m1, m2);
-        p1.x = bf16x2_scale(p1.x, m1, m2);
-        p0.y = bf16x2_scale(p0.y, m1, m2 * 0.0625f);
-        p1.y = bf16x2_scale(p1.y, m1, m2 * 0.0625f);
+        if constexpr (X8) {
+            p0.x = bf16x2_scale(__byte_perm(v.x, v.y, 0x5410), m1, m2);
+            p0.y = bf16x2_scale(__byte_perm(v.x, v.y, 0x7632), m1, m2);
+            p1.x = bf16x2_scale(__byte_perm(v.z, v.w, 0x5410), m1, m2);
+            p1.y = bf16x2_scale(__byte_perm(v.z, v.w, 0x7632), m1, m2);
+        } else {
+            p0.x = __byte_perm(v.x, v.z, 0x5410);
+            p0.y = __byte_perm(v.x, v.z, 0x7632);
+            p1.x = __byte_perm(v.y, v.w, 0x5410);
+            p1.y = __byte_perm(v.y, v.w, 0x7632);
+            p0.x = bf16x2_scale(p0.x, m1, m2);
+            p1.x = bf16x2_scale(p1.x, m1, m2);
+            p0.y = bf16x2_scale(p0.y, m1, m2 * 0.0625f);
+            p1.y = bf16x2_scale(p1.y, m1, m2 * 0.0625f);
+        }
         if constexpr (LM) {
             const size_t li = (static_cast<size_t>(gl) * 4 + i) * 4 * BT + n * 4 + tt;
             reinterpret_cast<uint4*>(xs)[li] = make_uint4(p0.x, p0.y, p1.x, p1.y);
@@ -537,6 +553,25 @@ __global__ void q4_tile_kernel(const uint8_t* __restrict__ codes, const uint16_t
         v = make_uint4(w[0], w[1], w[2], w[3]);
     }
     *reinterpret_cast<uint4*>(tiled + rec * kRecBytes + piece * 16) = v;
+}
+
+// The int8 head's tiled copy: one thread per 16-byte piece of a 2,048-byte record (128 pieces):
+// piece 64h + 2l + e holds row 16j + l/4 + 8h, columns 128g + 32(l%4) + 16e .. +15.
+__global__ void q8_tile_kernel(const int8_t* __restrict__ codes, int N, int K, uint8_t* __restrict__ tiled,
+                               int64_t pieces) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= pieces) return;
+    const int G = K >> 7;
+    const int64_t rec = idx >> 7;
+    const int piece = static_cast<int>(idx & 127);
+    const int j = static_cast<int>(rec / G);
+    const int g = static_cast<int>(rec - static_cast<int64_t>(j) * G);
+    const int h = piece >> 6, l = (piece >> 1) & 31, e = piece & 1;
+    const int row = 16 * j + (l >> 2) + 8 * h;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row < N)
+        v = *reinterpret_cast<const uint4*>(codes + static_cast<size_t>(row) * K + g * 128 + (l & 3) * 32 + e * 16);
+    *reinterpret_cast<uint4*>(tiled + rec * kRec8Bytes + h * 1024 + l * 32 + e * 16) = v;
 }
 
 // ================================================================== work lists
@@ -984,7 +1019,7 @@ struct PrepParams {
     PrepJob j[kMaxMats];
 };
 
-template <int BT>
+template <int BT, bool X8 = false>
 __global__ void __launch_bounds__(256) q4_xprep_kernel(const __grid_constant__ PrepParams p) {
     __shared__ unsigned colmax[8];
     // The tile kernel after this one may start at once: it streams weights (read-only) until its
@@ -992,8 +1027,8 @@ __global__ void __launch_bounds__(256) q4_xprep_kernel(const __grid_constant__ P
     allow_dependents();
     grid_dependency_wait();  // x may be the previous kernel's output
     const PrepJob& j = p.j[blockIdx.x];
-    stage_x<BT, true>(j.x, j.K, p.B, 0, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, 256,
-                      [] { __syncthreads(); });
+    stage_x<BT, true, SyncThreads, X8>(j.x, j.K, p.B, 0, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, 256,
+                                       SyncThreads{});
 }
 
 // q4_tiles_ring_kernel: one CTA per SM, persistent over a list of independent matrices, no
@@ -1209,24 +1244,74 @@ struct FlatParams {
     const uint4* xf;    // otherwise: prepared activations (layout LM) ...
     const float* S;     // ... group sums divided by the column factors
     const float* fac;   // ... column factors
-    float* y;
+    float* y;           // may be null (int8 head: only the argmax wanted)
+    const uint16_t* rscale;  // int8 head: fp16 scale per row
+    int2* cand;         // int8 head, when not null: per CTA and batch column the best (value bits, row)
     int N, K, B;
-    int T;  // tiles
+    int T;   // tiles
+    int pf;  // int8 head: records of the run requested into L2 ahead of the loads (int4: kFlatPf)
+    int pad;
 };
 
-template <int WARPS, int S, int BT, bool XS>
+// Argmax order: NaN above every number (lowest index first among NaNs), then larger values, then
+// the lower index among equal values (numpy's argmax).  A total order, so any visiting order gives
+// the same winner.
+__device__ __forceinline__ bool ranks_above(float v, int i, float bv, int bi) {
+    const bool vn = v != v, bn = bv != bv;
+    if (vn || bn) return vn && (!bn || i < bi);
+    return v > bv || (v == bv && i < bi);
+}
+
+
+// ---- int8 head operands (Q8).  An int8 code c becomes the byte c + 128 by flipping its top bit;
+// a byte m in the low 8 bits of a bf16 with exponent field 0 or 1 is exactly m * 2^-133 (as for
+// the int4 codes), so one LOP3 turns bytes 0 and 2 of a word into an mma operand pair, and a shift
+// and a LOP3 bytes 1 and 3.  The offset is removed per record (128-column group g):
+// acc += c_g - 128 S_g, so that the running sum keeps the size of the result (summing the
+// offset terms over a whole row first makes the tensor-core sums about 80 times larger than
+// the result and their rounding visible); y = acc f scale.
+__device__ __forceinline__ uint32_t q8_lo(uint32_t w) { return (w & 0x00FF00FFu) ^ 0x00800080u; }
+__device__ __forceinline__ uint32_t q8_hi(uint32_t w) { return ((w >> 8) & 0x00FF00FFu) ^ 0x00800080u; }
+
+// c = the record's 16 rows x 8 columns over 128 k of (code + 128) x.  ra/rb: the lane's 32 code
+// bytes of rows q and q+8 (k = 32t .. 32t+31 of the group); xv[j]: mma 2j (x, y) and 2j+1 (z, w)
+// fragments.
+__device__ __forceinline__ void q8_dot(const uint4& ra0, const uint4& ra1, const uint4& rb0, const uint4& rb1,
+                                       const uint4 (&xv)[4], float (&c)[4]) {
+    const uint32_t wa[8] = {ra0.x, ra0.y, ra0.z, ra0.w, ra1.x, ra1.y, ra1.z, ra1.w};
+    const uint32_t wb[8] = {rb0.x, rb0.y, rb0.z, rb0.w, rb1.x, rb1.y, rb1.z, rb1.w};
+    float c2[4];  // two chains (mma 0-3 and 4-7), added at the end: a fixed order
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        float (&d)[4] = m < 4 ? c : c2;
+        const uint32_t b0 = (m & 1) ? xv[m >> 1].z : xv[m >> 1].x;
+        const uint32_t b1 = (m & 1) ? xv[m >> 1].w : xv[m >> 1].y;
+        if (m == 0 || m == 4)
+            mma_bf16_m16n8k16_zc(d, q8_lo(wa[m]), q8_lo(wb[m]), q8_hi(wa[m]), q8_hi(wb[m]), b0, b1);
+        else
+            mma_bf16_m16n8k16(d, q8_lo(wa[m]), q8_lo(wb[m]), q8_hi(wa[m]), q8_hi(wb[m]), b0, b1);
+    }
+    c[0] += c2[0];
+    c[1] += c2[1];
+    c[2] += c2[2];
+    c[3] += c2[3];
+}
+
+template <int WARPS, int S, int BT, bool XS, bool Q8 = false>
 __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_constant__ FlatParams p) {
     static_assert(S >= 2, "ring depth");
+    constexpr int kRec = Q8 ? kRec8Bytes : kRecBytes;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int ticket[WARPS];
     __shared__ unsigned colmax[8];
+    __shared__ int2 wbest[Q8 ? WARPS : 1][8];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int t = lane & 3, q = lane >> 2;
     const int B = p.B;
     const int G = p.K >> 7;
-    unsigned char* ring = smem + static_cast<size_t>(warp) * S * kRecBytes;
-    float4* part = reinterpret_cast<float4*>(smem + static_cast<size_t>(WARPS) * S * kRecBytes);  // [WARPS][2][32]
+    unsigned char* ring = smem + static_cast<size_t>(warp) * S * kRec;
+    float4* part = reinterpret_cast<float4*>(smem + static_cast<size_t>(WARPS) * S * kRec);  // [WARPS][2][32]
     unsigned char* xsm = reinterpret_cast<unsigned char*>(part + WARPS * 2 * 32);
     if (threadIdx.x < WARPS) ticket[threadIdx.x] = 0;
 
@@ -1243,24 +1328,33 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
     const int n = u + (warp < e ? 1 : 0);
 
     // ---- loading side
-    const uint8_t* ld_ptr = p.tiled + (static_cast<size_t>(t0) * G + r0) * kRecBytes + 16 * lane;
+    const int lane_off = Q8 ? 32 * lane : 16 * lane;
+    const int pf = Q8 ? p.pf : kFlatPf;
+    const uint8_t* ld_ptr = p.tiled + (static_cast<size_t>(t0) * G + r0) * kRec + lane_off;
     int ld_left = n;
-    if (lane == 0 && n > 0) prefetch_l2_bulk(ld_ptr, static_cast<uint32_t>(min(n, kFlatPf) * kRecBytes));
+    if (lane == 0 && n > 0 && pf > 0) prefetch_l2_bulk(ld_ptr, static_cast<uint32_t>(min(n, pf) * kRec));
     auto issue = [&](int slot_off) {
         if (ld_left > 0) {
-            if (lane == 0 && ld_left > kFlatPf)
-                prefetch_l2_bulk(ld_ptr + static_cast<size_t>(kFlatPf) * kRecBytes, kRecBytes);
-            unsigned char* dst = ring + slot_off + 16 * lane;
-            cp_async16(dst, ld_ptr);
-            cp_async16(dst + 512, ld_ptr + 512);
-            if (lane < 4) cp_async16(dst + 1024, ld_ptr + 1024);
-            ld_ptr += kRecBytes;
+            if (lane == 0 && pf > 0 && ld_left > pf)
+                prefetch_l2_bulk(ld_ptr + static_cast<size_t>(pf) * kRec, kRec);
+            unsigned char* dst = ring + slot_off + lane_off;
+            if constexpr (Q8) {
+                cp_async16(dst, ld_ptr);
+                cp_async16(dst + 16, ld_ptr + 16);
+                cp_async16(dst + 1024, ld_ptr + 1024);
+                cp_async16(dst + 1040, ld_ptr + 1040);
+            } else {
+                cp_async16(dst, ld_ptr);
+                cp_async16(dst + 512, ld_ptr + 512);
+                if (lane < 4) cp_async16(dst + 1024, ld_ptr + 1024);
+            }
+            ld_ptr += kRec;
             --ld_left;
         }
         cp_async_commit();
     };
 #pragma unroll
-    for (int s = 0; s < S - 1; ++s) issue(s * kRecBytes);  // weights are read-only: before the wait
+    for (int s = 0; s < S - 1; ++s) issue(s * kRec);  // weights are read-only: before the wait
 
     grid_dependency_wait();  // x (or its prepared copy) comes from the kernel before
     allow_dependents();
@@ -1272,8 +1366,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
         uint2* xs = reinterpret_cast<uint2*>(xsm);
         float* ssum = reinterpret_cast<float*>(xsm + static_cast<size_t>(G) * 256 * BT);
         float* fs = ssum + G * 8;
-        stage_x<BT, true>(p.x, p.K, B, 0, G, xs, ssum, fs, colmax, static_cast<int>(threadIdx.x), WARPS * 32,
-                          [] { __syncthreads(); });
+        stage_x<BT, true, SyncThreads, Q8>(p.x, p.K, B, 0, G, xs, ssum, fs, colmax, static_cast<int>(threadIdx.x),
+                                           WARPS * 32, SyncThreads{});
         __syncthreads();
         xf = reinterpret_cast<const uint4*>(xs);
         Sb = ssum;
@@ -1284,12 +1378,12 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
         Sb = p.S;
         fac = p.fac;
     }
-    auto ldx4 = [&](const uint4* a) -> uint4 {
-        if constexpr (XS) return *a;
+    auto ldx4 = [&](const uint4* a) -> uint4 {  // XS: explicit shared-memory loads
+        if constexpr (XS) return lds128(reinterpret_cast<const unsigned char*>(a));
         else return ld_dep_u4(a);
     };
     auto ldx2 = [&](const float* a) -> uint2 {
-        if constexpr (XS) return *reinterpret_cast<const uint2*>(a);
+        if constexpr (XS) return lds64(reinterpret_cast<const unsigned char*>(a));
         else return ld_dep_u2(a);
     };
     auto ldf = [&](const float* a) -> float {
@@ -1308,17 +1402,44 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
     const uint4* xg = xf + xlane + g * (16 * BT);
     const float* Sg = Sb + 2 * t + g * 8;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int rd = 0, prev = (S - 1) * kRecBytes;
+    int rd = 0, prev = (S - 1) * kRec;
+    float bv0 = -__int_as_float(0x7f800000), bv1 = bv0;  // Q8 argmax: best of columns c0, c1 so far
+    int bi0 = 0x7fffffff, bi1 = 0x7fffffff;
 
     auto store_y = [&](const float (&a)[4]) {
         const int ra = 16 * (t0 + tile) + q, rbw = ra + 8;
+        float v[4];
+        if constexpr (Q8) {
+            const float sca = ra < p.N ? half_bits_to_f32(ld_nc_u16(p.rscale + ra)) : 0.f;
+            const float scb = rbw < p.N ? half_bits_to_f32(ld_nc_u16(p.rscale + rbw)) : 0.f;
+            v[0] = (a[0] * f0) * sca;
+            v[1] = (a[1] * f1) * sca;
+            v[2] = (a[2] * f0) * scb;
+            v[3] = (a[3] * f1) * scb;
+            if (p.cand) {
+                if (ra < p.N) {
+                    if (ranks_above(v[0], ra, bv0, bi0)) { bv0 = v[0]; bi0 = ra; }
+                    if (ranks_above(v[1], ra, bv1, bi1)) { bv1 = v[1]; bi1 = ra; }
+                }
+                if (rbw < p.N) {
+                    if (ranks_above(v[2], rbw, bv0, bi0)) { bv0 = v[2]; bi0 = rbw; }
+                    if (ranks_above(v[3], rbw, bv1, bi1)) { bv1 = v[3]; bi1 = rbw; }
+                }
+            }
+        } else {
+            v[0] = a[0] * f0;
+            v[1] = a[1] * f1;
+            v[2] = a[2] * f0;
+            v[3] = a[3] * f1;
+        }
+        if (p.y == nullptr) return;
         if (ra < p.N) {
-            if (c0 < B) p.y[static_cast<size_t>(c0) * p.N + ra] = a[0] * f0;
-            if (c1 < B) p.y[static_cast<size_t>(c1) * p.N + ra] = a[1] * f1;
+            if (c0 < B) p.y[static_cast<size_t>(c0) * p.N + ra] = v[0];
+            if (c1 < B) p.y[static_cast<size_t>(c1) * p.N + ra] = v[1];
         }
         if (rbw < p.N) {
-            if (c0 < B) p.y[static_cast<size_t>(c0) * p.N + rbw] = a[2] * f0;
-            if (c1 < B) p.y[static_cast<size_t>(c1) * p.N + rbw] = a[3] * f1;
+            if (c0 < B) p.y[static_cast<size_t>(c0) * p.N + rbw] = v[2];
+            if (c1 < B) p.y[static_cast<size_t>(c1) * p.N + rbw] = v[3];
         }
     };
     auto flush = [&](int ge) {  // segment [gs, ge) of `tile` is complete
@@ -1357,29 +1478,46 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
         uint4 xv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) xv[j] = ldx4(xg + j * (4 * BT));
-        const uint2 sv = ldx2(Sg);
         const unsigned char* rec = ring + rd;
-        const uint4 qa = lds128(rec + 16 * lane);
-        const uint4 qb = lds128(rec + 512 + 16 * lane);
-        const uint2 sc = lds64(rec + 1024 + 8 * q);
-        issue(prev);  // S - 1 records ahead, into the slot read one step ago
-        prev = rd;
-        rd = rd + kRecBytes == S * kRecBytes ? 0 : rd + kRecBytes;
-        float cc[4];
-        group_dot_x4(qa, qb, xv, cc);
-        const float Sx = __uint_as_float(sv.x), Sy = __uint_as_float(sv.y);
-        const float sa = half_bits_to_f32(sc.x), ma = half_bits_to_f32(sc.x >> 16);
-        const float sb = half_bits_to_f32(sc.y), mb = half_bits_to_f32(sc.y >> 16);
-        acc[0] = fmaf(sa, cc[0], acc[0]);
-        acc[0] = fmaf(ma, Sx, acc[0]);
-        acc[1] = fmaf(sa, cc[1], acc[1]);
-        acc[1] = fmaf(ma, Sy, acc[1]);
-        acc[2] = fmaf(sb, cc[2], acc[2]);
-        acc[2] = fmaf(mb, Sx, acc[2]);
-        acc[3] = fmaf(sb, cc[3], acc[3]);
-        acc[3] = fmaf(mb, Sy, acc[3]);
+        if constexpr (Q8) {
+            const uint2 sv = ldx2(Sg);
+            const uint4 ra0 = lds128(rec + 32 * lane), ra1 = lds128(rec + 32 * lane + 16);
+            const uint4 rb0 = lds128(rec + 1024 + 32 * lane), rb1 = lds128(rec + 1024 + 32 * lane + 16);
+            issue(prev);  // S - 1 records ahead, into the slot read one step ago
+            prev = rd;
+            rd = rd + kRec == S * kRec ? 0 : rd + kRec;
+            float cc[4];
+            q8_dot(ra0, ra1, rb0, rb1, xv, cc);
+            const float Sx = __uint_as_float(sv.x), Sy = __uint_as_float(sv.y);
+            acc[0] += fmaf(-128.f, Sx, cc[0]);
+            acc[1] += fmaf(-128.f, Sy, cc[1]);
+            acc[2] += fmaf(-128.f, Sx, cc[2]);
+            acc[3] += fmaf(-128.f, Sy, cc[3]);
+            Sg += 8;
+        } else {
+            const uint2 sv = ldx2(Sg);
+            const uint4 qa = lds128(rec + 16 * lane);
+            const uint4 qb = lds128(rec + 512 + 16 * lane);
+            const uint2 sc = lds64(rec + 1024 + 8 * q);
+            issue(prev);  // S - 1 records ahead, into the slot read one step ago
+            prev = rd;
+            rd = rd + kRec == S * kRec ? 0 : rd + kRec;
+            float cc[4];
+            group_dot_x4(qa, qb, xv, cc);
+            const float Sx = __uint_as_float(sv.x), Sy = __uint_as_float(sv.y);
+            const float sa = half_bits_to_f32(sc.x), ma = half_bits_to_f32(sc.x >> 16);
+            const float sb = half_bits_to_f32(sc.y), mb = half_bits_to_f32(sc.y >> 16);
+            acc[0] = fmaf(sa, cc[0], acc[0]);
+            acc[0] = fmaf(ma, Sx, acc[0]);
+            acc[1] = fmaf(sa, cc[1], acc[1]);
+            acc[1] = fmaf(ma, Sy, acc[1]);
+            acc[2] = fmaf(sb, cc[2], acc[2]);
+            acc[2] = fmaf(mb, Sx, acc[2]);
+            acc[3] = fmaf(sb, cc[3], acc[3]);
+            acc[3] = fmaf(mb, Sy, acc[3]);
+            Sg += 8;
+        }
         xg += 16 * BT;
-        Sg += 8;
         ++g;
         if (g == G || i == n - 1) {
             flush(g);
@@ -1392,14 +1530,86 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
         }
     }
     cp_async_wait<0>();
+    if constexpr (Q8) {
+        if (p.cand) {  // this CTA's best row per batch column (columns >= B are never read)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {  // lanes with the same t hold the same two columns
+                const float ov0 = __shfl_xor_sync(0xffffffffu, bv0, o), ov1 = __shfl_xor_sync(0xffffffffu, bv1, o);
+                const int oi0 = __shfl_xor_sync(0xffffffffu, bi0, o), oi1 = __shfl_xor_sync(0xffffffffu, bi1, o);
+                if (ranks_above(ov0, oi0, bv0, bi0)) { bv0 = ov0; bi0 = oi0; }
+                if (ranks_above(ov1, oi1, bv1, bi1)) { bv1 = ov1; bi1 = oi1; }
+            }
+            if (q == 0) {
+                wbest[warp][c0] = make_int2(__float_as_int(bv0), bi0);
+                wbest[warp][c1] = make_int2(__float_as_int(bv1), bi1);
+            }
+            __syncthreads();
+            if (threadIdx.x < 8) {
+                float bv = -__int_as_float(0x7f800000);
+                int bi = 0x7fffffff;
+                for (int w2 = 0; w2 < WARPS; ++w2) {
+                    const int2 cv = wbest[w2][threadIdx.x];
+                    if (ranks_above(__int_as_float(cv.x), cv.y, bv, bi)) { bv = __int_as_float(cv.x); bi = cv.y; }
+                }
+                p.cand[blockIdx.x * 8 + threadIdx.x] = make_int2(__float_as_int(bv), bi);
+            }
+        }
+    }
+}
+
+// The int8 head's argmax: per batch column the best of the per-CTA candidates of q4_flat_kernel
+// ([n_cta][8]).  One CTA of 256 threads: thread t takes candidates t, t + 256, ... (all of column
+// t % 8; their loads are independent), then lanes of one column combine by shuffles and the
+// warps through shared memory.  ranks_above is a total order, so the combining order is free.
+__global__ void __launch_bounds__(256) q8_argmax_final(const int2* cand, int n_cta, int B, int32_t* idx) {
+    __shared__ int2 wb[8][8];
+    grid_dependency_wait();  // the candidates come from the kernel before
+    allow_dependents();      // whatever follows writes only after its own wait
+    const int tid = static_cast<int>(threadIdx.x);
+    float bv = -__int_as_float(0x7f800000);
+    int bi = 0x7fffffff;
+    const int n = n_cta * 8;
+    uint2 v[5];
+#pragma unroll
+    for (int u = 0; u < 5; ++u) {  // n <= 5 * 256 for up to 160 CTAs; the rest below
+        const int i = tid + u * 256;
+        v[u] = i < n ? ld_dep_u2(cand + i) : make_uint2(__float_as_uint(bv), 0x7fffffffu);
+    }
+#pragma unroll
+    for (int u = 0; u < 5; ++u) {
+        const float cv = __uint_as_float(v[u].x);
+        const int ci = static_cast<int>(v[u].y);
+        if (ranks_above(cv, ci, bv, bi)) { bv = cv; bi = ci; }
+    }
+    for (int i = tid + 5 * 256; i < n; i += 256) {
+        const uint2 w = ld_dep_u2(cand + i);
+        if (ranks_above(__uint_as_float(w.x), static_cast<int>(w.y), bv, bi)) {
+            bv = __uint_as_float(w.x);
+            bi = static_cast<int>(w.y);
+        }
+    }
+#pragma unroll
+    for (int o = 8; o < 32; o <<= 1) {  // lanes with the same lane % 8 hold the same column
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ranks_above(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    const int lane = tid & 31, warp = tid >> 5;
+    if (lane < 8) wb[warp][lane] = make_int2(__float_as_int(bv), bi);
+    __syncthreads();
+    if (tid < B) {
+        bv = __int_as_float(wb[0][tid].x);
+        bi = wb[0][tid].y;
+        for (int w = 1; w < 8; ++w)
+            if (ranks_above(__int_as_float(wb[w][tid].x), wb[w][tid].y, bv, bi)) {
+                bv = __int_as_float(wb[w][tid].x);
+                bi = wb[w][tid].y;
+            }
+        idx[tid] = bi == 0x7fffffff ? 0 : bi;
+    }
 }
 
 // ================================================================== argmax
-__device__ __forceinline__ bool ranks_above(float v, int i, float bv, int bi) {
-    const bool vn = v != v, bn = bv != bv;
-    if (vn || bn) return vn && (!bn || i < bi);
-    return v > bv || (v == bv && i < bi);
-}
 
 __device__ __forceinline__ float4 ld_dep_f4(const float4* p) {
     float4 r;
@@ -1820,8 +2030,9 @@ unsigned wait_limit() {
 // ---- tile kernel: activation prep and streaming as two launches
 // Prepared activations of matrix i live at ws + (sum of prep_bytes of the matrices before it)
 // (or at ws for every matrix when `shared` lists run one matrix per launch).
+// x8: prepare with the int8 head's pairing (q8_head) instead of the int4 one.
 q4_status tiles_prepare(const Knobs& k, const q4_matrix* mats, int n, const uint16_t* const* X, int B, void* ws,
-                        bool independent, int dev, cudaStream_t stream) {
+                        bool independent, int dev, cudaStream_t stream, bool x8 = false) {
     const int bt = batch_tile(k, 5, B);
     const int per_launch = independent ? kMaxMats : 1;
     size_t off = 0;
@@ -1844,8 +2055,10 @@ q4_status tiles_prepare(const Knobs& k, const q4_matrix* mats, int n, const uint
             j.fac = j.S + G * 8;
         }
         using PrepFn = void (*)(PrepParams);
-        const PrepFn pf = bt == 1 ? q4_xprep_kernel<1> : bt == 2 ? q4_xprep_kernel<2> : bt == 4 ? q4_xprep_kernel<4>
-                                                                                               : q4_xprep_kernel<8>;
+        const PrepFn pf = x8 ? (bt == 1 ? q4_xprep_kernel<1, true> : bt == 2 ? q4_xprep_kernel<2, true>
+                                : bt == 4 ? q4_xprep_kernel<4, true> : q4_xprep_kernel<8, true>)
+                             : (bt == 1 ? q4_xprep_kernel<1> : bt == 2 ? q4_xprep_kernel<2>
+                                : bt == 4 ? q4_xprep_kernel<4> : q4_xprep_kernel<8>);
         const q4_status s = launch(pf, dev, static_cast<unsigned>(cnt), 256u, 0, stream, k.pdl, pp);
         if (s != Q4_OK) return s;
     }
@@ -2262,6 +2475,121 @@ extern "C" q4_status q4_gemm_skinny_noalloc(const q4_matrix* W, const uint16_t* 
     s = tiles_prepare(k, W, 1, &X, B, scratch, true, dev, st);
     if (s != Q4_OK) return s;
     return tiles_stream(k, W, 1, &Y, B, scratch, true, dev, sms, st);
+}
+
+// ------------------------------------------------------------------ the int8 head
+namespace {
+// warps per CTA (16 with 4 ring slots, or 24 with 3) and L2 prefetch distance of the int8 head
+int q8_warps() { return env_int("Q4_Q8W", 16) == 24 ? 24 : 16; }
+int q8_slots(int w) { return w == 24 ? 3 : 4; }
+int q8_pf() {
+    const int v = env_int("Q4_Q8PF", 0);
+    return v < 0 || v > 64 ? 0 : v;
+}
+size_t q8_smem(int64_t K, int bt, bool xs) {
+    const int w = q8_warps();
+    return static_cast<size_t>(w) * q8_slots(w) * kRec8Bytes + static_cast<size_t>(w) * 2 * 32 * 16 +
+           (xs ? prep_bytes(K, bt) : 0);
+}
+bool q8_xs(int64_t K, int bt) { return q8_smem(K, bt, true) <= kSmemLimit; }
+size_t q8_cand_bytes(int grid) { return align256(static_cast<size_t>(grid) * 8 * sizeof(int2)); }
+size_t q8_ws(int64_t N, int64_t K, int bt, int sms) {
+    return q8_cand_bytes(flat_grid(N, sms)) + (q8_xs(K, bt) ? 0 : align256(prep_bytes(K, bt)));
+}
+int q8_bt(int B) { return B <= 1 ? 1 : (B <= 2 ? 2 : (B <= 4 ? 4 : 8)); }
+}  // namespace
+
+extern "C" size_t q8_tiled_bytes(int64_t N, int64_t K) {
+    if (check_shape(N, K) != Q4_OK) return 0;
+    return static_cast<size_t>((N + 15) / 16) * static_cast<size_t>(K / 128) * kRec8Bytes;
+}
+
+extern "C" q4_status q8_tile(const q8_matrix* W, void* tiled, size_t tiled_bytes, void* stream) {
+    if (!W || !W->codes || !tiled) return Q4_ERR_INVALID_ARG;
+    q4_status s = check_shape(W->N, W->K);
+    if (s != Q4_OK) return s;
+    if (!aligned(W->codes, 16) || !aligned(tiled, 16)) return Q4_ERR_MISALIGNED;
+    if (tiled_bytes < q8_tiled_bytes(W->N, W->K)) return Q4_ERR_WORKSPACE;
+    if (fault_injected()) return Q4_ERR_CUDA;
+    const int64_t pieces = ((W->N + 15) / 16) * (W->K / 128) * 128;
+    const unsigned grid = static_cast<unsigned>((pieces + 255) / 256);
+    q8_tile_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        W->codes, static_cast<int>(W->N), static_cast<int>(W->K), static_cast<uint8_t*>(tiled), pieces);
+    return cudaPeekAtLastError() == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+}
+
+extern "C" size_t q8_head_workspace_bytes(int64_t N, int64_t K, int B) {
+    if (check_shape(N, K) != Q4_OK || B < 1 || B > kMaxB) return 0;
+    const int sms = device_sm_count(nullptr);
+    if (sms <= 0) return 0;
+    return q8_ws(N, K, q8_bt(B), sms);
+}
+
+extern "C" q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float* Y, int32_t* idx, void* ws,
+                             size_t ws_bytes, void* stream) {
+    if (!W || !W->tiled || !W->scales || !X || (!Y && !idx)) return Q4_ERR_INVALID_ARG;
+    if (B < 1 || B > kMaxB) return Q4_ERR_INVALID_ARG;
+    q4_status st = check_shape(W->N, W->K);
+    if (st != Q4_OK) return st;
+    if (!aligned(W->tiled, 16) || !aligned(W->scales, 2) || !aligned(X, 16) || (Y && !aligned(Y, 4)) ||
+        (idx && !aligned(idx, 4)))
+        return Q4_ERR_MISALIGNED;
+    int dev = 0;
+    const int sms = device_sm_count(&dev);
+    if (sms <= 0) return Q4_ERR_CUDA;
+    const int bt = q8_bt(B);
+    const size_t need = q8_ws(W->N, W->K, bt, sms);
+    if (!ws || ws_bytes < need) return Q4_ERR_WORKSPACE;
+    if (!aligned(ws, 16)) return Q4_ERR_MISALIGNED;
+    if (fault_injected()) return Q4_ERR_CUDA;
+    const Knobs k = knobs();
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int grid = flat_grid(W->N, sms);
+    const bool xs = q8_xs(W->K, bt);
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    FlatParams fp;
+    std::memset(&fp, 0, sizeof fp);
+    fp.tiled = static_cast<const uint8_t*>(W->tiled);
+    fp.x = X;
+    fp.y = Y;
+    fp.rscale = W->scales;
+    fp.cand = idx ? reinterpret_cast<int2*>(w) : nullptr;
+    fp.N = static_cast<int>(W->N);
+    fp.K = static_cast<int>(W->K);
+    fp.B = B;
+    fp.T = static_cast<int>((W->N + 15) / 16);
+    if (!xs) {
+        unsigned char* pw = w + q8_cand_bytes(grid);
+        q4_matrix m{};
+        m.N = W->N;
+        m.K = W->K;
+        st = tiles_prepare(k, &m, 1, &X, B, pw, true, dev, cs, true);
+        if (st != Q4_OK) return st;
+        const size_t G = static_cast<size_t>(W->K / 128);
+        fp.xf = reinterpret_cast<const uint4*>(pw);
+        fp.S = reinterpret_cast<const float*>(pw + G * 256 * bt);
+        fp.fac = fp.S + G * 8;
+    }
+    fp.pf = q8_pf();
+    const int qw = q8_warps();
+    using FlatFn = void (*)(FlatParams);
+    FlatFn ff;
+    if (qw == 24 && xs)
+        ff = bt == 1 ? q4_flat_kernel<24, 3, 1, true, true> : bt == 2 ? q4_flat_kernel<24, 3, 2, true, true>
+           : bt == 4 ? q4_flat_kernel<24, 3, 4, true, true> : q4_flat_kernel<24, 3, 8, true, true>;
+    else if (qw == 24)
+        ff = bt == 1 ? q4_flat_kernel<24, 3, 1, false, true> : bt == 2 ? q4_flat_kernel<24, 3, 2, false, true>
+           : bt == 4 ? q4_flat_kernel<24, 3, 4, false, true> : q4_flat_kernel<24, 3, 8, false, true>;
+    else if (xs)
+        ff = bt == 1 ? q4_flat_kernel<16, 4, 1, true, true> : bt == 2 ? q4_flat_kernel<16, 4, 2, true, true>
+           : bt == 4 ? q4_flat_kernel<16, 4, 4, true, true> : q4_flat_kernel<16, 4, 8, true, true>;
+    else
+        ff = bt == 1 ? q4_flat_kernel<16, 4, 1, false, true> : bt == 2 ? q4_flat_kernel<16, 4, 2, false, true>
+           : bt == 4 ? q4_flat_kernel<16, 4, 4, false, true> : q4_flat_kernel<16, 4, 8, false, true>;
+    st = launch(ff, dev, static_cast<unsigned>(grid), static_cast<unsigned>(qw * 32), q8_smem(W->K, bt, xs), cs,
+                k.pdl, fp);
+    if (st != Q4_OK || !idx) return st;
+    return launch(q8_argmax_final, dev, 1u, 256u, 0, cs, k.pdl, static_cast<const int2*>(fp.cand), grid, B, idx);
 }
 
 extern "C" q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream) {

@@ -99,6 +99,55 @@ bool pack_rows(const float* w, int64_t K, int64_t r_begin, int64_t r_end,
 
 }  // namespace
 
+namespace {
+// The int8 output head (per-row symmetric, see q4.h): s = fp16(max |w| / 127), rounded once from
+// double; code = clamp(nearbyint(w / s), -127, 127) with the stored scale (round-half-even);
+// s == 0 gives code 0.  False for a non-finite weight or a scale that overflows fp16.
+bool pack_rows8(const float* w, int64_t K, int64_t r0, int64_t r1, int8_t* codes, uint16_t* scales) {
+    for (int64_t r = r0; r < r1; ++r) {
+        const float* row = w + r * K;
+        double mx = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double v = row[k];
+            if (!std::isfinite(v)) return false;
+            mx = std::fabs(v) > mx ? std::fabs(v) : mx;
+        }
+        bool ovf = false;
+        const uint16_t sbits = half_bits_from_double(mx / 127.0, &ovf);
+        if (ovf) return false;
+        scales[r] = sbits;
+        const double s = double_from_half_bits(sbits);
+        int8_t* out = codes + r * K;
+        for (int64_t k = 0; k < K; ++k) {
+            double q = s == 0.0 ? 0.0 : std::nearbyint(static_cast<double>(row[k]) / s);
+            q = q < -127.0 ? -127.0 : (q > 127.0 ? 127.0 : q);
+            out[k] = static_cast<int8_t>(q);
+        }
+    }
+    return true;
+}
+}  // namespace
+
+extern "C" q4_status q8_pack_host(const float* w, int64_t N, int64_t K, int8_t* codes, uint16_t* scales,
+                                  int n_threads) {
+    if (!w || !codes || !scales || N <= 0) return Q4_ERR_INVALID_ARG;
+    if (K <= 0 || K % 128 != 0) return Q4_ERR_UNSUPPORTED_SHAPE;
+    int T = n_threads > 0 ? n_threads : static_cast<int>(std::thread::hardware_concurrency());
+    if (T < 1) T = 1;
+    if (static_cast<int64_t>(T) > N) T = static_cast<int>(N);
+    std::atomic<bool> ok{true};
+    std::vector<std::thread> pool;
+    pool.reserve(T);
+    for (int t = 0; t < T; ++t) {
+        const int64_t a = N * t / T, b = N * (t + 1) / T;
+        pool.emplace_back([=, &ok] {
+            if (!pack_rows8(w, K, a, b, codes, scales)) ok = false;
+        });
+    }
+    for (auto& th : pool) th.join();
+    return ok ? Q4_OK : Q4_ERR_INVALID_ARG;
+}
+
 extern "C" q4_status q4_pack_host(const float* w, int64_t N, int64_t K,
                                   uint8_t* codes, uint16_t* scales, uint16_t* mins,
                                   int n_threads) {

@@ -1,0 +1,78 @@
+"""CPU tests of the int8 output head's host side: the packer against the oracle, bit for bit,
+and the argument checks of q8_tile / q8_head that run before any launch.  No GPU needed.
+
+The format (rumik-oss-1 write-up, "Steps 9-10: streaming to the speaker": the head in int8;
+"Step 2": torchao's int8 weights) is one symmetric fp16 scale per output row.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle.q8_oracle as Q8
+import synthetic
+import int4_weight_only_q4_gb300 as q4
+from int4_weight_only_q4_gb300 import _lib
+
+
+@pytest.mark.parametrize("N,K,seed,threads", [(1, 128, 0, 1), (37, 384, 1, 3), (300, 3072, 2, 0),
+                                              (5, 16384, 3, 2)])
+def test_pack_matches_oracle(N, K, seed, threads):
+    w, _ = synthetic.random_shape_problem(N, K, 1, seed=seed, outliers=True)
+    c, s = q4.pack_int8_host(w, threads)
+    oc, osb = Q8.quantise_rows(w)
+    assert np.array_equal(s, osb)
+    assert np.array_equal(c, oc)
+
+
+def test_pack_special_rows():
+    w = np.zeros((5, 256), np.float32)
+    w[0, :6] = [127.0, 2.5, -3.5, 0.5, -0.5, 126.5]          # ties to even at scale 1
+    w[1, :3] = [1.25 * 127 * 2.0 ** -24, -127 * 2.0 ** -24, 0]  # subnormal scale: clamp at 127
+    w[2] = (np.arange(256) - 128) * 0.0078125                 # ramp
+    w[4] = -3.0                                               # constant row
+    c, s = q4.pack_int8_host(w)
+    oc, osb = Q8.quantise_rows(w)
+    assert np.array_equal(s, osb) and np.array_equal(c, oc)
+    assert c[0, :6].tolist() == [127, 2, -4, 0, 0, 126]
+    assert c[1, 0] == 127 and s[3] == 0 and not c[3].any()
+
+
+def test_pack_rejects_bad_input():
+    L = _lib.lib
+    w = np.zeros((2, 128), np.float32)
+    codes = np.empty((2, 128), np.int8)
+    sc = np.empty(2, np.uint16)
+    w[1, 3] = np.inf
+    assert L.q8_pack_host(w.ctypes.data, 2, 128, codes.ctypes.data, sc.ctypes.data, 1) == _lib.Q4_ERR_INVALID_ARG
+    w[1, 3] = 65504.0 * 127 * 1.01
+    assert L.q8_pack_host(w.ctypes.data, 2, 128, codes.ctypes.data, sc.ctypes.data, 1) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q8_pack_host(w.ctypes.data, 2, 100, codes.ctypes.data, sc.ctypes.data, 1) == \
+        _lib.Q4_ERR_UNSUPPORTED_SHAPE
+    assert L.q8_pack_host(None, 2, 128, codes.ctypes.data, sc.ctypes.data, 1) == _lib.Q4_ERR_INVALID_ARG
+
+
+def test_tiled_bytes():
+    L = _lib.lib
+    assert L.q8_tiled_bytes(65536, 3072) == 4096 * 24 * 2048
+    assert L.q8_tiled_bytes(17, 256) == 2 * 2 * 2048
+    assert L.q8_tiled_bytes(16, 100) == 0
+
+
+def test_head_argument_checks_before_any_launch():
+    L = _lib.lib
+    fake = 1 << 20  # 16-byte aligned dummy addresses: nothing is dereferenced before these checks
+    m = _lib.q8_matrix(fake, fake, 1000, 1024, fake)
+    ok_y, ok_i = fake, fake
+    assert L.q8_head(ctypes.byref(m), fake, 0, ok_y, ok_i, fake, 1 << 20, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q8_head(ctypes.byref(m), fake, 9, ok_y, ok_i, fake, 1 << 20, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q8_head(ctypes.byref(m), fake, 1, None, None, fake, 1 << 20, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q8_head(ctypes.byref(m), None, 1, ok_y, ok_i, fake, 1 << 20, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q8_head(ctypes.byref(m), fake + 2, 1, ok_y, ok_i, fake, 1 << 20, None) == _lib.Q4_ERR_MISALIGNED
+    bad = _lib.q8_matrix(fake, fake, 1000, 1000, fake)
+    assert L.q8_head(ctypes.byref(bad), fake, 1, ok_y, ok_i, fake, 1 << 20, None) == \
+        _lib.Q4_ERR_UNSUPPORTED_SHAPE
+    no_tiled = _lib.q8_matrix(fake, fake, 1000, 1024, None)
+    assert L.q8_head(ctypes.byref(no_tiled), fake, 1, ok_y, ok_i, fake, 1 << 20, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q8_tile(ctypes.byref(m), None, 0, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q8_tile(ctypes.byref(m), fake, 16, None) == _lib.Q4_ERR_WORKSPACE
