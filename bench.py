@@ -375,6 +375,7 @@ def run_ours(args):
     fused_sus = fused_sustained(q4, torch, mats, dev, args)
     # the int8 output head with the argmax fused in
     head8 = int8_head(q4, torch, dev, args)
+    samp = sampler_bench(q4, torch, dev, args)
 
     # end to end through the public API with pinned host buffers
     e2e = end_to_end(q4, torch, g1, xs1, dev, max(10, args.steps // 20), barrier)
@@ -390,7 +391,7 @@ def run_ours(args):
         "decode_step_us": dec_us, "decode_step_chained_launches_us": chained_us, "step_with_head_us": {"b1": round(ms1 * 1e3, 2), "b8": round(ms8 * 1e3, 2)},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "roofline": roof, "fused_projection_sustained": fused_sus, "fused_gemv_single_call": fused_single,
-        "int8_head_65536x3072": head8,
+        "int8_head_65536x3072": head8, "sampler_topk_gumbel": samp,
         "gen_seconds": round(gen_s, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -549,6 +550,41 @@ def int8_head(q4, torch, dev, args):
     peak, src = measured_peak_gbs()
     out["frac_b1_argmax_only"] = round(out["b1_argmax_only"]["GB/s"] / peak, 4)
     out["kernel"] = "q4_flat_kernel<16, 4, BT, true, true> + q8_argmax_final (8 calls per CUDA graph)"
+    return out
+
+
+def sampler_bench(q4, torch, dev, args):
+    """Top-k (k = 50) Gumbel-max sampling over 65,536 logits per row (q4_sample_topk), B = 1 and 8:
+    20 calls per CUDA graph, microseconds per call."""
+    N = synthetic.SHAPES["head"][0]
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed + 777)
+    for B in (1, 8):
+        Y = torch.randn((B, N), device=dev, generator=gen) * 3
+        u = torch.rand((B, 50), device=dev, generator=gen).clamp_(1e-12, 1 - 1e-7)
+        noise = -torch.log(-torch.log(u))
+        tok = torch.empty((B,), dtype=torch.int32, device=dev)
+        side = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(side):
+            q4.sample_topk(Y, 50, 1.25, noise, token=tok, stream=side)
+            side.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(20):
+                    q4.sample_topk(Y, 50, 1.25, noise, token=tok, stream=side)
+        for _ in range(3):
+            g.replay()
+        n = max(10, args.steps // 100)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out[f"b{B}_us_per_call"] = round(1e3 * e0.elapsed_time(e1) / (n * 20), 3)
+    out["kernel"] = "q4_sample_kernel (one 1024-thread CTA per row; k = 50, N = 65,536)"
     return out
 
 

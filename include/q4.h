@@ -282,6 +282,26 @@ size_t q4_noalloc_scratch_bytes(void);
  */
 q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream);
 
+/*
+ * q4_sample_topk -- top-k sampling with the Gumbel-max trick over logits
+ * (rumik-oss-1 write-up, "Step 4": top-k sampling on the GPU with the
+ * Gumbel-max trick; "Steps 9-10": the top k found by sorting 64-bit keys that
+ * pack the float bits with the index).  Per batch row b of Y [B, N] (device
+ * fp32): rank the logits -- NaN above every number, larger first, the lower
+ * index first among equal values (the q4_argmax_f32 order) -- and keep the first
+ * k; score rank r as fp32(fp32(Y[b, i_r] * inv_temperature) + noise[b, r]), two
+ * rounded binary32 operations (never fused); token[b] = i_r of the best score
+ * (NaN first, ties to the lower rank).  The caller supplies the randomness:
+ * noise [B, k] (device fp32), Gumbel(0, 1) noise for ranks 0..k-1.
+ *   k     1 <= k <= min(N, 1024);  inv_temperature > 0 and finite.
+ *   token device int32 [B];  topk device int32 [B, k] (the ranked indices) or NULL.
+ * One CTA of 1024 threads per row, no workspace.  Q4_ERR_INVALID_ARG for null
+ * pointers or out-of-range k, B (1..65535), N or inv_temperature;
+ * Q4_ERR_MISALIGNED unless every pointer is 4-byte aligned.
+ */
+q4_status q4_sample_topk(const float* Y, int B, int64_t N, int k, float inv_temperature, const float* noise,
+                         int32_t* token, int32_t* topk, void* stream);
+
 /* ------------------------------------------------------------------------
  * The int8 output head.  The rumik-oss-1 write-up keeps every projection in
  * int4 except the output head ("Steps 9-10: streaming to the speaker": the

@@ -26,7 +26,7 @@ MAX_B = 8
 __all__ = ["GROUP", "MAX_B", "Q4Error", "QuantizedMatrix", "Workspace", "pack_host", "plan",
            "workspace_bytes", "decode_step_workspace_bytes", "tiled_bytes", "gemv", "gemm_skinny", "decode_step",
            "argmax", "device_status", "DecodeStepGraph", "step_workspace_bytes", "step_prepare", "step_stream",
-           "gemm_skinny_noalloc", "pack_int8_host", "Int8Head",
+           "gemm_skinny_noalloc", "pack_int8_host", "Int8Head", "sample_topk",
            "header_functions", "lib"]
 
 
@@ -318,6 +318,24 @@ class Int8Head:
         check(lib.q8_head(ctypes.byref(m), _ptr(X), B, _ptr(Y) if logits else None, _ptr(idx) if argmax else None,
                           ws_p, ws_n, _stream_ptr(stream)), "q8_head")
         return (Y if logits else None), (idx if argmax else None)
+
+
+def sample_topk(Y: torch.Tensor, k: int, inv_temperature: float, noise: torch.Tensor,
+                token: torch.Tensor | None = None, topk: torch.Tensor | None = None, return_topk: bool = False,
+                stream=None):
+    """Top-k Gumbel-max sampling per row of fp32 logits [B, N] with caller-supplied noise [B, k]
+    (q4_sample_topk).  Returns token int32 [B] (and the ranked top-k indices [B, k])."""
+    if Y.dtype != torch.float32 or not Y.is_contiguous() or noise.dtype != torch.float32 or not noise.is_contiguous():
+        raise TypeError("logits and noise must be contiguous float32 CUDA tensors")
+    Y2 = Y if Y.dim() == 2 else Y.view(1, -1)
+    B, N = Y2.shape
+    if token is None:
+        token = torch.empty((B,), dtype=torch.int32, device=Y.device)
+    if return_topk and topk is None:
+        topk = torch.empty((B, k), dtype=torch.int32, device=Y.device)
+    check(lib.q4_sample_topk(_ptr(Y2), B, N, int(k), float(inv_temperature), _ptr(noise), _ptr(token),
+                             _ptr(topk) if topk is not None else None, _stream_ptr(stream)), "q4_sample_topk")
+    return (token, topk) if return_topk else token
 
 
 class DecodeStepGraph:

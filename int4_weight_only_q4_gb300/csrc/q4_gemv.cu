@@ -56,6 +56,7 @@
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -1682,6 +1683,207 @@ __global__ void __launch_bounds__(1024) q4_argmax_kernel(const float* __restrict
     }
 }
 
+// ================================================================== top-k Gumbel-max sampler
+// q4_sample_kernel: one CTA of 1024 threads per batch row of logits.  The top k follow the argmax
+// order (NaN above every number, larger first, lower index first among equal values): a 32-bit
+// key that grows with that order (rank_key) and, packed with the complemented index below it, a
+// 64-bit key that is unique and sorts the same way.  (1) A radix select over the key's four bytes,
+// most significant first, finds the k-th best key T: elements above T all belong to the top k, and
+// of those equal to T the lowest-index ones fill the rest.  (2) The k candidates are gathered into
+// shared memory and sorted by their 64-bit keys (bitonic, descending), which gives the ranks.
+// (3) Thread r scores rank r as fp32(fp32(y * inv_temperature) + noise[r]) -- two rounded
+// operations, never fused -- and the best score (NaN first, ties to the lower rank) picks the token.
+constexpr int kSampleThreads = 1024;
+constexpr int kSampleMaxK = 1024;
+
+__device__ __forceinline__ uint32_t rank_key(float v) {
+    if (v != v) return 0xFFFFFFFFu;  // NaN: above every number
+    uint32_t b = __float_as_uint(v);
+    if ((b & 0x7FFFFFFFu) == 0) b = 0;  // -0 and +0 are equal values
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kSampleThreads) q4_sample_kernel(const float* Y, int N, int k, float inv_t,
+                                                                   const float* noise, int32_t* token,
+                                                                   int32_t* topk) {
+    __shared__ unsigned hist[256];
+    __shared__ unsigned long long cand[kSampleMaxK];
+    __shared__ unsigned sh_prefix, sh_remain, sh_ties, sh_count, sh_tie_base;
+    __shared__ unsigned warp_sum[32];
+    __shared__ float best_s[32];
+    __shared__ int best_r[32];
+    grid_dependency_wait();  // the logits are usually the previous kernel's output
+    allow_dependents();
+    const int tid = static_cast<int>(threadIdx.x);
+    const int lane = tid & 31, warp = tid >> 5;
+    const float* row = Y + static_cast<size_t>(blockIdx.x) * N;
+    constexpr int U = 8;  // loads in flight per thread
+    auto key_at = [&](int i) -> uint32_t { return rank_key(ld_dep_f32(row + i)); };
+    // fn(index, value) over the whole row: VEC reads 16-byte words (row 16-byte aligned, N % 4 == 0),
+    // U independent loads in flight per thread, coalesced across the block
+    auto for_row = [&](auto&& fn) {
+        if constexpr (VEC) {
+            const float4* row4 = reinterpret_cast<const float4*>(row);
+            const int n4 = N >> 2;
+            for (int base = tid; base < n4; base += U * kSampleThreads) {
+                float4 v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = base + u * kSampleThreads;
+                    v[u] = j < n4 ? ld_dep_f4(row4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = base + u * kSampleThreads;
+                    if (j < n4) {
+                        fn(4 * j, v[u].x);
+                        fn(4 * j + 1, v[u].y);
+                        fn(4 * j + 2, v[u].z);
+                        fn(4 * j + 3, v[u].w);
+                    }
+                }
+            }
+        } else {
+            for (int base = tid; base < N; base += U * kSampleThreads) {
+                float v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = base + u * kSampleThreads;
+                    v[u] = i < N ? ld_dep_f32(row + i) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = base + u * kSampleThreads;
+                    if (i < N) fn(i, v[u]);
+                }
+            }
+        }
+    };
+
+    // (1) radix select
+    uint32_t prefix = 0, mask = 0;
+    unsigned remain = static_cast<unsigned>(k);
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        if (tid < 256) hist[tid] = 0;
+        __syncthreads();
+        // lanes of a warp that fall into the same bin add once (most keys share a few high bytes,
+        // and one shared-memory atomic per element would serialise on those bins)
+        for_row([&](int, float v) {
+            const uint32_t key = rank_key(v);
+            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        });
+        __syncthreads();
+        if (tid == 0) {
+            unsigned above = 0;  // matching elements with a larger digit
+            int d = 255;
+            for (; d > 0; --d) {
+                if (above + hist[d] >= remain) break;
+                above += hist[d];
+            }
+            sh_prefix = prefix | (static_cast<uint32_t>(d) << shift);
+            sh_remain = remain - above;
+            sh_ties = hist[d];
+        }
+        __syncthreads();
+        prefix = sh_prefix;
+        remain = sh_remain;
+        mask |= 0xFFu << shift;
+    }
+    const uint32_t T = prefix;
+    const unsigned take_ties = remain;           // elements equal to T to take (>= 1)
+    const unsigned above_T = static_cast<unsigned>(k) - take_ties;
+    const bool all_ties = sh_ties == take_ties;  // (sh_ties: elements equal to T)
+
+    // (2) gather: keys above T anywhere in [0, above_T); ties in [above_T, k), lowest index first
+    if (tid == 0) { sh_count = 0; sh_tie_base = 0; }
+    __syncthreads();
+    for_row([&](int i, float v) {
+        const uint32_t key = rank_key(v);
+        const unsigned long long packed =
+            (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
+        if (key > T) cand[atomicAdd(&sh_count, 1u)] = packed;
+        else if (key == T && all_ties) cand[above_T + atomicAdd(&sh_tie_base, 1u)] = packed;
+    });
+    if (!all_ties) {
+        // more elements equal T than needed: walk the row in index order, 1024 at a time, and give
+        // each tie its rank among ties by a block-wide exclusive scan
+        __syncthreads();
+        unsigned running = 0;
+        for (int base = 0; base < N && running < take_ties; base += kSampleThreads) {
+            const int i = base + tid;
+            const unsigned flag = (i < N && key_at(i) == T) ? 1u : 0u;
+            const unsigned bal = __ballot_sync(0xffffffffu, flag);
+            if (lane == 0) warp_sum[warp] = __popc(bal);
+            __syncthreads();
+            unsigned before = 0, total = 0;
+            for (int w = 0; w < 32; ++w) {
+                const unsigned c = warp_sum[w];
+                if (w < warp) before += c;
+                total += c;
+            }
+            const unsigned rank = running + before + __popc(bal & ((1u << lane) - 1u));
+            if (flag && rank < take_ties)
+                cand[above_T + rank] =
+                    (static_cast<unsigned long long>(T) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
+            running += total;
+            __syncthreads();
+        }
+    }
+    // pad to a power of two with the smallest key and sort descending (bitonic)
+    int P = 1;
+    while (P < k) P <<= 1;
+    for (int i = k + tid; i < P; i += kSampleThreads) cand[i] = 0ull;
+    __syncthreads();
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < P; i += kSampleThreads) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;  // descending runs where the size bit is clear
+                    const unsigned long long a = cand[i], c = cand[j];
+                    if (desc ? (a < c) : (a > c)) {
+                        cand[i] = c;
+                        cand[j] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    // (3) scores and the token
+    float s = -__int_as_float(0x7f800000);
+    int r = 0x7fffffff;
+    int my_idx = 0;
+    if (tid < k) {
+        my_idx = static_cast<int>(~static_cast<uint32_t>(cand[tid] & 0xFFFFFFFFull));
+        if (topk) topk[static_cast<size_t>(blockIdx.x) * k + tid] = my_idx;
+        const float v = ld_dep_f32(row + my_idx);
+        s = __fadd_rn(__fmul_rn(v, inv_t), ld_dep_f32(noise + static_cast<size_t>(blockIdx.x) * k + tid));
+        r = tid;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, s, o);
+        const int orr = __shfl_xor_sync(0xffffffffu, r, o);
+        if (ranks_above(os, orr, s, r)) { s = os; r = orr; }
+    }
+    if (lane == 0) { best_s[warp] = s; best_r[warp] = r; }
+    __syncthreads();
+    if (warp == 0) {
+        s = best_s[lane];
+        r = best_r[lane];
+        for (int o = 16; o > 0; o >>= 1) {
+            const float os = __shfl_xor_sync(0xffffffffu, s, o);
+            const int orr = __shfl_xor_sync(0xffffffffu, r, o);
+            if (ranks_above(os, orr, s, r)) { s = os; r = orr; }
+        }
+        if (lane == 0)
+            token[blockIdx.x] = static_cast<int32_t>(~static_cast<uint32_t>(cand[r] & 0xFFFFFFFFull));
+    }
+}
+
 // ================================================================== host
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
@@ -1927,8 +2129,10 @@ bool smem_attr_set(Fn fn, int dev) {
     for (int i = 0; i < n_done; ++i)
         if (done[i].fn == key && done[i].dev == dev) return true;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit)) !=
-        cudaSuccess)
+        cudaSuccess) {
+        (void)cudaGetLastError();  // not sticky: clear it so that later checks do not see it
         return false;
+    }
     if (n_done < 512) done[n_done++] = Entry{key, dev};
     return true;
 }
@@ -1937,7 +2141,9 @@ template <typename Fn, typename... Args>
 q4_status launch(Fn fn, int dev, unsigned grid, unsigned block, size_t smem, cudaStream_t stream, bool pdl,
                  Args... args) {
     if (fault_injected()) return Q4_ERR_CUDA;
-    if (!smem_attr_set(fn, dev)) return Q4_ERR_CUDA;
+    // only launches past the default 48 KB need the raised limit (which, with a kernel's static
+    // shared memory, must stay under the per-block maximum)
+    if (smem > 48 * 1024 && !smem_attr_set(fn, dev)) return Q4_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
@@ -2590,6 +2796,24 @@ extern "C" q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float
                 k.pdl, fp);
     if (st != Q4_OK || !idx) return st;
     return launch(q8_argmax_final, dev, 1u, 256u, 0, cs, k.pdl, static_cast<const int2*>(fp.cand), grid, B, idx);
+}
+
+extern "C" q4_status q4_sample_topk(const float* Y, int B, int64_t N, int k, float inv_temperature,
+                                    const float* noise, int32_t* token, int32_t* topk, void* stream) {
+    if (!Y || !noise || !token || B < 1 || B > 65535 || N < 1 || N > 0x7fffffffLL) return Q4_ERR_INVALID_ARG;
+    if (k < 1 || k > kSampleMaxK || k > N) return Q4_ERR_INVALID_ARG;
+    if (!(inv_temperature > 0.f) || !std::isfinite(inv_temperature)) return Q4_ERR_INVALID_ARG;
+    if (!aligned(Y, 4) || !aligned(noise, 4) || !aligned(token, 4) || (topk && !aligned(topk, 4)))
+        return Q4_ERR_MISALIGNED;
+    if (fault_injected()) return Q4_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4_ERR_CUDA;
+    const bool vec = aligned(Y, 16) && (N % 4) == 0;
+    const Knobs kn = knobs();
+    auto fn = vec ? q4_sample_kernel<true> : q4_sample_kernel<false>;
+    return launch(fn, dev, static_cast<unsigned>(B), static_cast<unsigned>(kSampleThreads), 0,
+                  static_cast<cudaStream_t>(stream), kn.pdl, Y, static_cast<int>(N), k, inv_temperature, noise, token,
+                  topk);
 }
 
 extern "C" q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream) {

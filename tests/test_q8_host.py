@@ -76,3 +76,17 @@ def test_head_argument_checks_before_any_launch():
     assert L.q8_head(ctypes.byref(no_tiled), fake, 1, ok_y, ok_i, fake, 1 << 20, None) == _lib.Q4_ERR_INVALID_ARG
     assert L.q8_tile(ctypes.byref(m), None, 0, None) == _lib.Q4_ERR_INVALID_ARG
     assert L.q8_tile(ctypes.byref(m), fake, 16, None) == _lib.Q4_ERR_WORKSPACE
+
+
+def test_sampler_argument_checks_before_any_launch():
+    L = _lib.lib
+    f = 1 << 20
+    assert L.q4_sample_topk(f, 1, 100, 0, 1.0, f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_sample_topk(f, 1, 100, 101, 1.0, f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_sample_topk(f, 1, 5000, 1025, 1.0, f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_sample_topk(f, 1, 100, 5, 0.0, f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_sample_topk(f, 1, 100, 5, float("inf"), f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_sample_topk(f, 1, 100, 5, float("nan"), f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_sample_topk(None, 1, 100, 5, 1.0, f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_sample_topk(f, 0, 100, 5, 1.0, f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_sample_topk(f + 2, 1, 100, 5, 1.0, f, f, None, None) == _lib.Q4_ERR_MISALIGNED
