@@ -1687,14 +1687,19 @@ __global__ void __launch_bounds__(1024) q4_argmax_kernel(const float* __restrict
 // q4_sample_kernel: one CTA of 1024 threads per batch row of logits.  The top k follow the argmax
 // order (NaN above every number, larger first, lower index first among equal values): a 32-bit
 // key that grows with that order (rank_key) and, packed with the complemented index below it, a
-// 64-bit key that is unique and sorts the same way.  (1) A radix select over the key's four bytes,
-// most significant first, finds the k-th best key T: elements above T all belong to the top k, and
-// of those equal to T the lowest-index ones fill the rest.  (2) The k candidates are gathered into
-// shared memory and sorted by their 64-bit keys (bitonic, descending), which gives the ranks.
+// 64-bit key that is unique and sorts the same way.  (1) Each thread keeps the 4 best keys of its
+// elements; the k-th best of those 4096 (a radix select in shared memory), tau, has at least k
+// elements at or above it, so the top k all lie at or above tau.  Every element >= tau is gathered
+// (one ballot per warp step) and, when they fit in kSampleCap, sorted by their 64-bit keys
+// (bitonic, descending) -- the first k are the ranked top k.  When they do not fit (long runs of
+// equal values), a radix select over the key's four bytes, most significant first, finds the k-th
+// best key T instead: elements above T all belong to the top k, and of those equal to T the
+// lowest-index ones fill the rest; those k are gathered and sorted.
 // (3) Thread r scores rank r as fp32(fp32(y * inv_temperature) + noise[r]) -- two rounded
 // operations, never fused -- and the best score (NaN first, ties to the lower rank) picks the token.
 constexpr int kSampleThreads = 1024;
 constexpr int kSampleMaxK = 1024;
+constexpr int kSampleCap = 2048;  // candidates held in shared memory (>= kSampleMaxK)
 
 __device__ __forceinline__ uint32_t rank_key(float v) {
     if (v != v) return 0xFFFFFFFFu;  // NaN: above every number
@@ -1708,7 +1713,8 @@ __global__ void __launch_bounds__(kSampleThreads) q4_sample_kernel(const float* 
                                                                    const float* noise, int32_t* token,
                                                                    int32_t* topk) {
     __shared__ unsigned hist[256];
-    __shared__ unsigned long long cand[kSampleMaxK];
+    __shared__ uint32_t sample[4 * kSampleThreads];
+    __shared__ unsigned long long cand[kSampleCap];
     __shared__ unsigned sh_prefix, sh_remain, sh_ties, sh_count, sh_tie_base;
     __shared__ unsigned warp_sum[32];
     __shared__ float best_s[32];
@@ -1761,97 +1767,184 @@ __global__ void __launch_bounds__(kSampleThreads) q4_sample_kernel(const float* 
         }
     };
 
-    // (1) radix select
-    uint32_t prefix = 0, mask = 0;
-    unsigned remain = static_cast<unsigned>(k);
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        if (tid < 256) hist[tid] = 0;
-        __syncthreads();
-        // lanes of a warp that fall into the same bin add once (most keys share a few high bytes,
-        // and one shared-memory atomic per element would serialise on those bins)
-        for_row([&](int, float v) {
-            const uint32_t key = rank_key(v);
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-        });
-        __syncthreads();
-        if (tid == 0) {
-            unsigned above = 0;  // matching elements with a larger digit
-            int d = 255;
-            for (; d > 0; --d) {
-                if (above + hist[d] >= remain) break;
-                above += hist[d];
-            }
-            sh_prefix = prefix | (static_cast<uint32_t>(d) << shift);
-            sh_remain = remain - above;
-            sh_ties = hist[d];
-        }
-        __syncthreads();
-        prefix = sh_prefix;
-        remain = sh_remain;
-        mask |= 0xFFu << shift;
-    }
-    const uint32_t T = prefix;
-    const unsigned take_ties = remain;           // elements equal to T to take (>= 1)
-    const unsigned above_T = static_cast<unsigned>(k) - take_ties;
-    const bool all_ties = sh_ties == take_ties;  // (sh_ties: elements equal to T)
-
-    // (2) gather: keys above T anywhere in [0, above_T); ties in [above_T, k), lowest index first
-    if (tid == 0) { sh_count = 0; sh_tie_base = 0; }
-    __syncthreads();
-    for_row([&](int i, float v) {
-        const uint32_t key = rank_key(v);
-        const unsigned long long packed =
-            (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
-        if (key > T) cand[atomicAdd(&sh_count, 1u)] = packed;
-        else if (key == T && all_ties) cand[above_T + atomicAdd(&sh_tie_base, 1u)] = packed;
-    });
-    if (!all_ties) {
-        // more elements equal T than needed: walk the row in index order, 1024 at a time, and give
-        // each tie its rank among ties by a block-wide exclusive scan
-        __syncthreads();
-        unsigned running = 0;
-        for (int base = 0; base < N && running < take_ties; base += kSampleThreads) {
-            const int i = base + tid;
-            const unsigned flag = (i < N && key_at(i) == T) ? 1u : 0u;
-            const unsigned bal = __ballot_sync(0xffffffffu, flag);
-            if (lane == 0) warp_sum[warp] = __popc(bal);
-            __syncthreads();
-            unsigned before = 0, total = 0;
-            for (int w = 0; w < 32; ++w) {
-                const unsigned c = warp_sum[w];
-                if (w < warp) before += c;
-                total += c;
-            }
-            const unsigned rank = running + before + __popc(bal & ((1u << lane) - 1u));
-            if (flag && rank < take_ties)
-                cand[above_T + rank] =
-                    (static_cast<unsigned long long>(T) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
-            running += total;
-            __syncthreads();
-        }
-    }
-    // pad to a power of two with the smallest key and sort descending (bitonic)
-    int P = 1;
-    while (P < k) P <<= 1;
-    for (int i = k + tid; i < P; i += kSampleThreads) cand[i] = 0ull;
-    __syncthreads();
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < P; i += kSampleThreads) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const bool desc = (i & size) == 0;  // descending runs where the size bit is clear
-                    const unsigned long long a = cand[i], c = cand[j];
-                    if (desc ? (a < c) : (a > c)) {
-                        cand[i] = c;
-                        cand[j] = a;
+    // bitonic sort, descending, of a[0..P) (P a power of two) by the whole block
+    auto sort_desc = [&](auto* a, int P) {
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < P; i += kSampleThreads) {
+                    const int j = i ^ stride;
+                    if (j > i) {
+                        const bool desc = (i & size) == 0;  // descending runs where the size bit is clear
+                        const auto x = a[i], y = a[j];
+                        if (desc ? (x < y) : (x > y)) {
+                            a[i] = y;
+                            a[j] = x;
+                        }
                     }
                 }
+                __syncthreads();
+            }
+        }
+    };
+    auto pack = [](uint32_t key, int i) {
+        return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
+    };
+    // warp 0: the digit d whose bin holds the remain-th largest counted key, scanning bins from 255
+    // down; lane l holds bins 255-8l .. 248-8l, a shuffle scan finds the crossing lane.  Writes
+    // sh_prefix (prefix | d << shift), sh_remain (remain minus the keys in higher bins), sh_ties.
+    auto select_digit = [&](uint32_t prefix, int shift, unsigned remain) {
+        if (warp != 0) return;
+        unsigned c[8], local = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c[j] = hist[255 - 8 * lane - j];
+            local += c[j];
+        }
+        unsigned incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const unsigned excl = incl - local;
+        if (excl < remain && remain <= incl) {
+            unsigned above = excl;
+            int j = 0;
+            for (; j < 7; ++j) {
+                if (above + c[j] >= remain) break;
+                above += c[j];
+            }
+            const int d = 255 - 8 * lane - j;
+            sh_prefix = prefix | (static_cast<uint32_t>(d) << shift);
+            sh_remain = remain - above;
+            sh_ties = c[j];
+        }
+    };
+
+    // (1) the 4 best keys of each thread's elements (0 sorts below every element's key)
+    {
+        uint32_t t4[4] = {0u, 0u, 0u, 0u};
+        for_row([&](int, float v) {
+            const uint32_t key = rank_key(v);
+            if (key > t4[3]) {
+                if (key > t4[0]) { t4[3] = t4[2]; t4[2] = t4[1]; t4[1] = t4[0]; t4[0] = key; }
+                else if (key > t4[1]) { t4[3] = t4[2]; t4[2] = t4[1]; t4[1] = key; }
+                else if (key > t4[2]) { t4[3] = t4[2]; t4[2] = key; }
+                else t4[3] = key;
+            }
+        });
+#pragma unroll
+        for (int m = 0; m < 4; ++m) sample[4 * tid + m] = t4[m];
+        if (tid == 0) sh_count = 0;
+        __syncthreads();
+    }
+    // tau = the k-th largest of the 4096 sampled keys: a radix select over them in shared memory
+    uint32_t tau;
+    {
+        uint32_t prefix = 0, mask = 0;
+        unsigned remain = static_cast<unsigned>(k);
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            if (tid < 256) hist[tid] = 0;
+            __syncthreads();
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t key = sample[m * kSampleThreads + tid];
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
             }
             __syncthreads();
+            select_digit(prefix, shift, remain);
+            __syncthreads();
+            prefix = sh_prefix;
+            remain = sh_remain;
+            mask |= 0xFFu << shift;
         }
+        tau = prefix;
     }
+    // gather every element at or above tau: one ballot and one shared counter step per warp step
+    for_row([&](int i, float v) {
+        const uint32_t key = rank_key(v);
+        const bool take = key >= tau;
+        const unsigned act = __activemask();
+        const unsigned bal = __ballot_sync(act, take);
+        const int leader = __ffs(act) - 1;
+        unsigned base = 0;
+        if (lane == leader && bal) base = atomicAdd(&sh_count, static_cast<unsigned>(__popc(bal)));
+        base = __shfl_sync(act, base, leader);
+        if (take) {
+            const unsigned pos = base + __popc(bal & ((1u << lane) - 1u));
+            if (pos < static_cast<unsigned>(kSampleCap)) cand[pos] = pack(key, i);
+        }
+    });
+    __syncthreads();
+    int n_cand = static_cast<int>(sh_count);
+    if (n_cand > kSampleCap) {  // too many to hold: radix select for the exact k-th best key
+        uint32_t prefix = 0, mask = 0;
+        unsigned remain = static_cast<unsigned>(k);
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            if (tid < 256) hist[tid] = 0;
+            __syncthreads();
+            for_row([&](int, float v) {
+                const uint32_t key = rank_key(v);
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            });
+            __syncthreads();
+            select_digit(prefix, shift, remain);
+            __syncthreads();
+            prefix = sh_prefix;
+            remain = sh_remain;
+            mask |= 0xFFu << shift;
+        }
+        const uint32_t T = prefix;
+        const unsigned take_ties = remain;           // elements equal to T to take (>= 1)
+        const unsigned above_T = static_cast<unsigned>(k) - take_ties;
+        const bool all_ties = sh_ties == take_ties;  // (sh_ties: elements equal to T)
+
+        // (2) gather: keys above T anywhere in [0, above_T); ties in [above_T, k), lowest index first
+        if (tid == 0) { sh_count = 0; sh_tie_base = 0; }
+        __syncthreads();
+        for_row([&](int i, float v) {
+            const uint32_t key = rank_key(v);
+            const unsigned long long packed =
+                (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
+            if (key > T) cand[atomicAdd(&sh_count, 1u)] = packed;
+            else if (key == T && all_ties) cand[above_T + atomicAdd(&sh_tie_base, 1u)] = packed;
+        });
+        if (!all_ties) {
+            // more elements equal T than needed: walk the row in index order, 1024 at a time, and give
+            // each tie its rank among ties by a block-wide exclusive scan
+            __syncthreads();
+            unsigned running = 0;
+            for (int base = 0; base < N && running < take_ties; base += kSampleThreads) {
+                const int i = base + tid;
+                const unsigned flag = (i < N && key_at(i) == T) ? 1u : 0u;
+                const unsigned bal = __ballot_sync(0xffffffffu, flag);
+                if (lane == 0) warp_sum[warp] = __popc(bal);
+                __syncthreads();
+                unsigned before = 0, total = 0;
+                for (int w = 0; w < 32; ++w) {
+                    const unsigned c = warp_sum[w];
+                    if (w < warp) before += c;
+                    total += c;
+                }
+                const unsigned rank = running + before + __popc(bal & ((1u << lane) - 1u));
+                if (flag && rank < take_ties)
+                    cand[above_T + rank] =
+                        (static_cast<unsigned long long>(T) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
+                running += total;
+                __syncthreads();
+            }
+        }
+        __syncthreads();
+        n_cand = k;
+    }
+    // pad to a power of two with the smallest key and sort descending: the first k are the top k
+    int P = 1;
+    while (P < n_cand) P <<= 1;
+    for (int i = n_cand + tid; i < P; i += kSampleThreads) cand[i] = 0ull;
+    __syncthreads();
+    sort_desc(cand, P);
 
     // (3) scores and the token
     float s = -__int_as_float(0x7f800000);
