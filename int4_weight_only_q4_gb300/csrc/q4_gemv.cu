@@ -56,6 +56,7 @@
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -1058,6 +1059,8 @@ struct TileMat {
 struct TileParams {
     int n_mats;
     int B;
+    int contiguous;  // 1: CTA c takes a record-balanced contiguous range of the whole tile list
+    int pad;
     TileMat m[kMaxMats];
 };
 
@@ -1078,17 +1081,40 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
     unsigned char* ring = smem + static_cast<size_t>(warp) * S * kRecBytes;
     if (threadIdx.x == 0) {
         int acc = 0;
-        for (int i = 0; i < p.n_mats; ++i) {
-            const TileMat& m = p.m[i];
-            prefix[i] = acc;
-            tfirst[i] = 0;
-            if (static_cast<int>(blockIdx.x) < m.row_blocks) {
-                const int T_all = (m.N + 15) >> 4;
-                const int rb = (static_cast<int>(blockIdx.x) + m.rot) % m.row_blocks;
-                const int t0 = static_cast<int>(static_cast<int64_t>(rb) * T_all / m.row_blocks);
-                const int t1 = static_cast<int>(static_cast<int64_t>(rb + 1) * T_all / m.row_blocks);
-                tfirst[i] = t0;
-                acc += t1 - t0;
+        if (p.contiguous) {
+            // the list's tiles, matrix after matrix, as one run of records; CTA c takes the tiles
+            // whose first record falls in [c R / grid, (c+1) R / grid)
+            int64_t R = 0;
+            for (int i = 0; i < p.n_mats; ++i) R += static_cast<int64_t>((p.m[i].N + 15) >> 4) * (p.m[i].K >> 7);
+            const int64_t nb = gridDim.x, c = blockIdx.x;
+            const int64_t lo = c * R / nb, hi = (c + 1) * R / nb;
+            int64_t cum = 0;
+            for (int i = 0; i < p.n_mats; ++i) {
+                const TileMat& m = p.m[i];
+                const int64_t T_all = (m.N + 15) >> 4, G = m.K >> 7;
+                // tiles t with cum + t G in [lo, hi)
+                int64_t t0 = lo > cum ? (lo - cum + G - 1) / G : 0;
+                int64_t t1 = hi > cum ? (hi - cum + G - 1) / G : 0;
+                t0 = t0 < T_all ? t0 : T_all;
+                t1 = t1 < T_all ? t1 : T_all;
+                prefix[i] = acc;
+                tfirst[i] = static_cast<int>(t0);
+                acc += static_cast<int>(t1 - t0);
+                cum += T_all * G;
+            }
+        } else {
+            for (int i = 0; i < p.n_mats; ++i) {
+                const TileMat& m = p.m[i];
+                prefix[i] = acc;
+                tfirst[i] = 0;
+                if (static_cast<int>(blockIdx.x) < m.row_blocks) {
+                    const int T_all = (m.N + 15) >> 4;
+                    const int rb = (static_cast<int>(blockIdx.x) + m.rot) % m.row_blocks;
+                    const int t0 = static_cast<int>(static_cast<int64_t>(rb) * T_all / m.row_blocks);
+                    const int t1 = static_cast<int>(static_cast<int64_t>(rb + 1) * T_all / m.row_blocks);
+                    tfirst[i] = t0;
+                    acc += t1 - t0;
+                }
             }
         }
         prefix[p.n_mats] = acc;
@@ -2011,6 +2037,7 @@ struct Knobs {
     bool pdl, rotate;
     int l2_ahead;      // direct kernel on L1: units prefetched into L2 ahead of the loads
     int tw, ts;        // tile kernel: warps per CTA and cp.async ring slots per warp
+    bool tile_contig;  // tile kernel: record-balanced contiguous shares of the whole list per CTA
 };
 
 Knobs knobs() {
@@ -2035,6 +2062,7 @@ Knobs knobs() {
     k.tw = env_int("Q4_TW", 32);
     if (k.tw != 16 && k.tw != 24) k.tw = 32;
     k.ts = k.tw == 16 ? 8 : k.tw == 24 ? 6 : 4;
+    k.tile_contig = env_int("Q4_TCONTIG", 0) != 0;
     return k;
 }
 
@@ -2375,6 +2403,7 @@ q4_status tiles_stream(const Knobs& k, const q4_matrix* mats, int n, float* cons
         std::memset(&tp, 0, sizeof tp);
         tp.n_mats = cnt;
         tp.B = B;
+        tp.contiguous = k.tile_contig ? 1 : 0;
         int grid = 1;
         for (int i = 0; i < cnt; ++i) {
             const q4_matrix& W = mats[base + i];
@@ -2395,6 +2424,26 @@ q4_status tiles_stream(const Knobs& k, const q4_matrix* mats, int n, float* cons
                                               : 0;
             if (m.row_blocks > grid) grid = m.row_blocks;
         }
+        // The order in which CTAs walk the list (not the arithmetic of any output): longest tiles
+        // first, then matrices grouped by shape in the order their shape first appears, so that the
+        // last tiles a CTA hands out are short and its warps finish together.
+        if (cnt > 1) {
+            int first[kMaxMats], idx[kMaxMats];
+            for (int i = 0; i < cnt; ++i) {
+                idx[i] = i;
+                first[i] = i;
+                for (int j = 0; j < i; ++j)
+                    if (tp.m[j].N == tp.m[i].N && tp.m[j].K == tp.m[i].K) { first[i] = first[j]; break; }
+            }
+            std::stable_sort(idx, idx + cnt, [&](int a, int b) {
+                if (tp.m[a].K != tp.m[b].K) return tp.m[a].K > tp.m[b].K;
+                return first[a] < first[b];
+            });
+            TileMat sorted[kMaxMats];
+            for (int i = 0; i < cnt; ++i) sorted[i] = tp.m[idx[i]];
+            for (int i = 0; i < cnt; ++i) tp.m[i] = sorted[i];
+        }
+        if (tp.contiguous) grid = sms;  // every CTA takes a share of the whole list
         using TilesFn = void (*)(TileParams);
         TilesFn tf = nullptr;
         const size_t smem = static_cast<size_t>(k.tw) * k.ts * kRecBytes;

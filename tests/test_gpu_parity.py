@@ -392,7 +392,8 @@ def test_decode_step_independent_and_chained_agree(q4):
     q4.device_status()
 
 
-@pytest.mark.parametrize("env", [{"Q4_TW": "16"}, {"Q4_TW": "24"}, {"Q4_TW": "32"}])
+@pytest.mark.parametrize("env", [{"Q4_TW": "16"}, {"Q4_TW": "24"}, {"Q4_TW": "32"}, {"Q4_TCONTIG": "1"},
+                                 {"Q4_TCONTIG": "0"}, {"Q4_TCONTIG": "1", "Q4_TW": "24"}])
 def test_tile_kernel_shapes(q4, monkeypatch, env):
     """Every warp count / ring depth of the tile kernel: oracle parity and batch invariance; the
     shapes share one arithmetic order, so they agree bit for bit with the default."""
