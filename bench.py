@@ -643,6 +643,36 @@ def run_profile_case(args) -> int:
     return 0
 
 
+def run_profile_small(args) -> int:
+    """Small cases for ncu: `--profile-head8` one int8-head call (65,536 x 3072, seeded random codes on
+    the device, B = --profile-batch, logits + argmax) after two warm-up calls; `--profile-sampler`
+    one top-k (k = 50) Gumbel-max sampling call over 65,536 logits after two warm-up calls."""
+    import torch
+    import int4_weight_only_q4_gb300 as q4
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed)
+    B = args.profile_batch
+    N, K, _ = synthetic.SHAPES["head"]
+    if args.profile_head8:
+        H = q4.Int8Head.from_device(torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev, generator=gen),
+                                    (torch.rand((N,), device=dev, generator=gen) * 1e-3 + 1e-4).half())
+        X = torch.randn((B, K), device=dev, generator=gen).to(torch.bfloat16)
+        for _ in range(3):
+            Y, idx = H(X)
+    else:
+        Y = torch.randn((B, N), device=dev, generator=gen) * 3
+        noise = torch.zeros((B, 50), device=dev)
+        for _ in range(3):
+            idx = q4.sample_topk(Y, 50, 1.0, noise)
+    torch.cuda.synchronize()
+    q4.device_status()
+    print(json.dumps({"profile_case": "int8 head" if args.profile_head8 else "sampler", "B": B,
+                      "idx": idx.cpu().tolist()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -655,9 +685,13 @@ def main():
     ap.add_argument("--profile-step", type=int, default=0,
                     help="run only a small profiling case of this many layers + the head, then exit")
     ap.add_argument("--profile-batch", type=int, default=1)
+    ap.add_argument("--profile-head8", action="store_true", help="run only a small int8-head case for ncu")
+    ap.add_argument("--profile-sampler", action="store_true", help="run only a small sampler case for ncu")
     args = ap.parse_args()
     if args.profile_step > 0:
         return run_profile_case(args)
+    if args.profile_head8 or args.profile_sampler:
+        return run_profile_small(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
