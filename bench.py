@@ -376,6 +376,7 @@ def run_ours(args):
     # the int8 output head with the argmax fused in
     head8 = int8_head(q4, torch, dev, args)
     samp = sampler_bench(q4, torch, dev, args)
+    prefill = prefill_bench(q4, torch, mats, dev, args)
 
     # end to end through the public API with pinned host buffers
     e2e = end_to_end(q4, torch, g1, xs1, dev, max(10, args.steps // 20), barrier)
@@ -391,7 +392,7 @@ def run_ours(args):
         "decode_step_us": dec_us, "decode_step_chained_launches_us": chained_us, "step_with_head_us": {"b1": round(ms1 * 1e3, 2), "b8": round(ms8 * 1e3, 2)},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "roofline": roof, "fused_projection_sustained": fused_sus, "fused_gemv_single_call": fused_single,
-        "int8_head_65536x3072": head8, "sampler_topk_gumbel": samp,
+        "int8_head_65536x3072": head8, "sampler_topk_gumbel": samp, "prefill_gemm": prefill,
         "gen_seconds": round(gen_s, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -585,6 +586,43 @@ def sampler_bench(q4, torch, dev, args):
         torch.cuda.synchronize()
         out[f"b{B}_us_per_call"] = round(1e3 * e0.elapsed_time(e1) / (n * 20), 3)
     out["kernel"] = "q4_sample_kernel (one 1024-thread CTA per row; k = 50, N = 65,536)"
+    return out
+
+
+def prefill_bench(q4, torch, mats, dev, args):
+    """The int4 prefill GEMM (q4_gemm_prefill) on the step's fused 25,088 x 3072 projection for
+    prompts of 128 and 512 tokens: microseconds per call (5 per CUDA graph) and TFLOP/s."""
+    W = next(m for m in mats if (m.N, m.K) == (25088, 3072))
+    out = {}
+    peak = json.load(open(PEAKS_FILE)).get("bf16_tflops") if os.path.exists(PEAKS_FILE) else None
+    for M in (128, 512):
+        X = torch.randn((M, W.K), device=dev).to(torch.bfloat16)
+        Y = torch.empty((M, W.N), device=dev)
+        ws = q4.Workspace(int(q4.lib.q4_prefill_workspace_bytes(W.K, M)), dev)
+        side = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(side):
+            q4.gemm_prefill(W, X, Y, ws, stream=side)
+            side.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(5):
+                    q4.gemm_prefill(W, X, Y, ws, stream=side)
+        for _ in range(3):
+            g.replay()
+        n = max(10, args.steps // 100)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / (n * 5)
+        tf = 2 * M * W.N * W.K / (us * 1e-6) / 1e12
+        out[f"m{M}"] = {"us_per_call": round(us, 2), "TFLOP/s": round(tf, 1),
+                        "frac_of_bf16_peak": round(tf / peak, 4) if peak else None}
+    out["kernel"] = "q4_xprep_kernel + q4_prefill_kernel (mma.sync m16n8k16 bf16, fused 25088x3072)"
+    out["bound"] = "tensor"
     return out
 
 

@@ -283,6 +283,22 @@ size_t q4_noalloc_scratch_bytes(void);
 q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream);
 
 /*
+ * q4_gemm_prefill -- Y[m, :] = W X[m, :] for a prompt of M tokens (the rumik-oss-1
+ * write-up, "Step 8: a prefill that stays int4": the weights stay int4, are
+ * unpacked a group at a time onto the tensor cores, and scale and minimum are
+ * applied to the result).  fp32 accumulation; a tensor-core GEMM (mma.sync),
+ * not bound by the weight bytes once M is large.
+ *   W   host pointer; W->tiled (device) is required.
+ *   X   device bf16 bits [M, K], 16-byte aligned;  Y device fp32 [M, N].
+ *   ws  device workspace of ws_bytes >= q4_prefill_workspace_bytes(K, M) (the
+ *       prepared activations; no initial content needed).
+ * Q4_ERR_INVALID_ARG for null pointers, no tiled copy or M outside 1..2^24.
+ */
+size_t q4_prefill_workspace_bytes(int64_t K, int64_t M);
+q4_status q4_gemm_prefill(const q4_matrix* W, const uint16_t* X, int64_t M, float* Y, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/*
  * q4_sample_topk -- top-k sampling with the Gumbel-max trick over logits
  * (rumik-oss-1 write-up, "Step 4": top-k sampling on the GPU with the
  * Gumbel-max trick; "Steps 9-10": the top k found by sorting 64-bit keys that

@@ -26,7 +26,7 @@ MAX_B = 8
 __all__ = ["GROUP", "MAX_B", "Q4Error", "QuantizedMatrix", "Workspace", "pack_host", "plan",
            "workspace_bytes", "decode_step_workspace_bytes", "tiled_bytes", "gemv", "gemm_skinny", "decode_step",
            "argmax", "device_status", "DecodeStepGraph", "step_workspace_bytes", "step_prepare", "step_stream",
-           "gemm_skinny_noalloc", "pack_int8_host", "Int8Head", "sample_topk",
+           "gemm_skinny_noalloc", "pack_int8_host", "Int8Head", "sample_topk", "gemm_prefill",
            "header_functions", "lib"]
 
 
@@ -318,6 +318,23 @@ class Int8Head:
         check(lib.q8_head(ctypes.byref(m), _ptr(X), B, _ptr(Y) if logits else None, _ptr(idx) if argmax else None,
                           ws_p, ws_n, _stream_ptr(stream)), "q8_head")
         return (Y if logits else None), (idx if argmax else None)
+
+
+def gemm_prefill(W: QuantizedMatrix, X: torch.Tensor, Y: torch.Tensor | None = None,
+                 workspace: Workspace | None = None, stream=None) -> torch.Tensor:
+    """Y [M, N] = X [M, K] W^T for a prompt of M tokens (q4_gemm_prefill, tensor-core GEMM)."""
+    X = _as_bf16(X)
+    X2 = X if X.dim() == 2 else X.view(1, -1)
+    M = X2.shape[0]
+    if Y is None:
+        Y = torch.empty((M, W.N), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = Workspace(int(lib.q4_prefill_workspace_bytes(W.K, M)), X.device)
+    ws_p, ws_n = _ws_args(workspace)
+    m = W.c_struct()
+    check(lib.q4_gemm_prefill(ctypes.byref(m), _ptr(X2), M, _ptr(Y), ws_p, ws_n, _stream_ptr(stream)),
+          "q4_gemm_prefill")
+    return Y
 
 
 def sample_topk(Y: torch.Tensor, k: int, inv_temperature: float, noise: torch.Tensor,

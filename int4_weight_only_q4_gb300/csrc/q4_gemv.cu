@@ -2003,6 +2003,163 @@ __global__ void __launch_bounds__(kSampleThreads) q4_sample_kernel(const float* 
     }
 }
 
+// ================================================================== int4 prefill GEMM
+// q4_prefill_kernel: Y[m, n] = sum_k w_hat[n, k] X[m, k] for a prompt of M tokens (the rumik-oss-1
+// write-up, "Step 8: a prefill that stays int4": the weights stay int4, a group is unpacked at a
+// time onto the tensor cores, and scale and minimum are applied to the result).  The tokens are
+// taken 8 at a time (a "token block"), each block prepared by q4_xprep_kernel exactly like a B = 8
+// decode activation (layout LM: scaled per token, group sums divided by the token factor).  A CTA of
+// WARPS warps covers WARPS 16-row tiles (one per warp) and TBS token blocks; for every 128-column
+// group it stages the TBS blocks' fragments in shared memory (cp.async, double-buffered) while each
+// warp loads its tile's record from the tiled copy, unpacks the codes once into 32 operand
+// registers and reuses them for 8 mma per token block, then folds scale and minimum in per block:
+// acc += scale c + min S'.  y = acc * the token's factor.  Tensor-bound for long prompts: 8 TBS mma
+// per 1,088-byte record.
+
+struct PrefillParams {
+    const uint8_t* tiled;
+    const unsigned char* prep;  // token block b's prepared activations at prep + b * prep_stride
+    size_t prep_stride;
+    float* y;                   // [M, N]
+    int N, K, M;
+};
+
+template <int WARPS, int TBS>
+__global__ void __launch_bounds__(WARPS * 32) q4_prefill_kernel(const __grid_constant__ PrefillParams p) {
+    constexpr int kXs = 4 * 32 * 16;  // one token block's fragments of one group: 2,048 bytes
+    __shared__ __align__(16) unsigned char xs[2][TBS][kXs];
+    __shared__ __align__(16) float ss[2][TBS][8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = lane & 3, q = lane >> 2;
+    const int G = p.K >> 7;
+    const int T = (p.N + 15) >> 4;
+    const int tile = blockIdx.x * WARPS + warp;
+    const bool active = tile < T;
+    const int nblk = (p.M + 7) >> 3;
+    const int tb0 = blockIdx.y * TBS;
+    const int nb = min(TBS, nblk - tb0);  // token blocks of this CTA
+
+    // stage group g's fragments and sums of the CTA's token blocks into buffer `buf`
+    auto stage = [&](int g, int buf) {
+        constexpr int kChunks = TBS * (kXs / 16 + 2);
+        for (int c = threadIdx.x; c < kChunks; c += WARPS * 32) {
+            const int b = c / (kXs / 16 + 2), r = c - b * (kXs / 16 + 2);
+            if (b >= nb) continue;
+            const unsigned char* base = p.prep + (tb0 + b) * p.prep_stride;
+            if (r < kXs / 16) {
+                cp_async16(&xs[buf][b][16 * r], base + static_cast<size_t>(g) * kXs + 16 * r);
+            } else {
+                const unsigned char* S = base + static_cast<size_t>(G) * kXs;  // G groups x 8 floats
+                cp_async16(&ss[buf][b][4 * (r - kXs / 16)], S + static_cast<size_t>(g) * 32 + 16 * (r - kXs / 16));
+            }
+        }
+        cp_async_commit();
+    };
+
+    grid_dependency_wait();  // the prepared activations come from the kernel before
+    allow_dependents();
+
+    float acc[TBS][4];
+#pragma unroll
+    for (int b = 0; b < TBS; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
+    const uint8_t* rec = p.tiled + static_cast<size_t>(active ? tile : 0) * G * kRecBytes;
+    // this warp's record of group g (read-only weights) is loaded one group ahead
+    uint4 nqa = make_uint4(0u, 0u, 0u, 0u), nqb = nqa;
+    uint2 nsc = make_uint2(0u, 0u);
+    if (active) {
+        nqa = ld_stream_u4(rec + 16 * lane);
+        nqb = ld_stream_u4(rec + 512 + 16 * lane);
+        nsc = ld_stream_u2(rec + 1024 + 8 * q);
+    }
+    stage(0, 0);
+#pragma unroll 1
+    for (int g = 0; g < G; ++g) {
+        const int buf = g & 1;
+        if (g + 1 < G) stage(g + 1, buf ^ 1);
+        else cp_async_commit();  // keep one group per step
+        // unpack group g's codes once into 32 operand registers; request group g+1's record
+        uint32_t A[8][4];
+        const uint4 qa = nqa, qb = nqb;
+        const uint2 sc = nsc;
+        if (active && g + 1 < G) {
+            const uint8_t* r = rec + static_cast<size_t>(g + 1) * kRecBytes;
+            nqa = ld_stream_u4(r + 16 * lane);
+            nqb = ld_stream_u4(r + 512 + 16 * lane);
+            nsc = ld_stream_u2(r + 1024 + 8 * q);
+        }
+        {
+            const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+            const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t wa8 = wa[i] >> 8, wb8 = wb[i] >> 8;
+                A[2 * i][0] = lo_nibbles(wa[i]);
+                A[2 * i][1] = lo_nibbles(wb[i]);
+                A[2 * i][2] = hi_nibbles(wa[i]);
+                A[2 * i][3] = hi_nibbles(wb[i]);
+                A[2 * i + 1][0] = lo_nibbles(wa8);
+                A[2 * i + 1][1] = lo_nibbles(wb8);
+                A[2 * i + 1][2] = hi_nibbles(wa8);
+                A[2 * i + 1][3] = hi_nibbles(wb8);
+            }
+        }
+        cp_async_wait<1>();  // group g's stage has landed
+        __syncthreads();
+        if (active) {
+            const float sa = half_bits_to_f32(sc.x), ma = half_bits_to_f32(sc.x >> 16);
+            const float sb = half_bits_to_f32(sc.y), mb = half_bits_to_f32(sc.y >> 16);
+#pragma unroll
+            for (int b = 0; b < TBS; ++b) {
+                if (b < nb) {
+                    uint4 xv[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) xv[j] = lds128(&xs[buf][b][(j * 32 + lane) * 16]);
+                    float c1[4], c2[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float (&d)[4] = i < 2 ? c1 : c2;
+                        if (i == 0 || i == 2)
+                            mma_bf16_m16n8k16_zc(d, A[2 * i][0], A[2 * i][1], A[2 * i][2], A[2 * i][3], xv[i].x, xv[i].y);
+                        else
+                            mma_bf16_m16n8k16(d, A[2 * i][0], A[2 * i][1], A[2 * i][2], A[2 * i][3], xv[i].x, xv[i].y);
+                        mma_bf16_m16n8k16(d, A[2 * i + 1][0], A[2 * i + 1][1], A[2 * i + 1][2], A[2 * i + 1][3],
+                                          xv[i].z, xv[i].w);
+                    }
+                    const float2 S = *reinterpret_cast<const float2*>(&ss[buf][b][2 * t]);
+                    acc[b][0] = fmaf(sa, c1[0] + c2[0], acc[b][0]);
+                    acc[b][0] = fmaf(ma, S.x, acc[b][0]);
+                    acc[b][1] = fmaf(sa, c1[1] + c2[1], acc[b][1]);
+                    acc[b][1] = fmaf(ma, S.y, acc[b][1]);
+                    acc[b][2] = fmaf(sb, c1[2] + c2[2], acc[b][2]);
+                    acc[b][2] = fmaf(mb, S.x, acc[b][2]);
+                    acc[b][3] = fmaf(sb, c1[3] + c2[3], acc[b][3]);
+                    acc[b][3] = fmaf(mb, S.y, acc[b][3]);
+                }
+            }
+        }
+        __syncthreads();  // buffer `buf` is restaged in the next step
+    }
+    cp_async_wait<0>();
+    if (!active) return;
+    const int ra = 16 * tile + q, rbw = ra + 8;
+#pragma unroll
+    for (int b = 0; b < TBS; ++b) {
+        if (b >= nb) continue;
+        const unsigned char* base = p.prep + (tb0 + b) * p.prep_stride;
+        const float* fac = reinterpret_cast<const float*>(base + static_cast<size_t>(G) * (kXs + 32));
+        const float f0 = ld_dep_f32(fac + 2 * t), f1 = ld_dep_f32(fac + 2 * t + 1);
+        const int m0 = 8 * (tb0 + b) + 2 * t, m1 = m0 + 1;
+        if (ra < p.N) {
+            if (m0 < p.M) p.y[static_cast<size_t>(m0) * p.N + ra] = acc[b][0] * f0;
+            if (m1 < p.M) p.y[static_cast<size_t>(m1) * p.N + ra] = acc[b][1] * f1;
+        }
+        if (rbw < p.N) {
+            if (m0 < p.M) p.y[static_cast<size_t>(m0) * p.N + rbw] = acc[b][2] * f0;
+            if (m1 < p.M) p.y[static_cast<size_t>(m1) * p.N + rbw] = acc[b][3] * f1;
+        }
+    }
+}
+
 // ================================================================== host
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
@@ -2823,6 +2980,89 @@ extern "C" q4_status q4_gemm_skinny_noalloc(const q4_matrix* W, const uint16_t* 
     s = tiles_prepare(k, W, 1, &X, B, scratch, true, dev, st);
     if (s != Q4_OK) return s;
     return tiles_stream(k, W, 1, &Y, B, scratch, true, dev, sms, st);
+}
+
+// ------------------------------------------------------------------ int4 prefill GEMM
+namespace {
+size_t prefill_ws(int64_t K, int64_t M) {
+    return static_cast<size_t>((M + 7) / 8) * prep_bytes(K, 8);
+}
+}  // namespace
+
+extern "C" size_t q4_prefill_workspace_bytes(int64_t K, int64_t M) {
+    if (K <= 0 || K % 128 != 0 || M < 1 || M > (1 << 24)) return 0;
+    return prefill_ws(K, M);
+}
+
+extern "C" q4_status q4_gemm_prefill(const q4_matrix* W, const uint16_t* X, int64_t M, float* Y, void* ws,
+                                     size_t ws_bytes, void* stream) {
+    if (!W || !W->tiled || !X || !Y || M < 1 || M > (1 << 24)) return Q4_ERR_INVALID_ARG;
+    q4_status st = check_shape(W->N, W->K);
+    if (st != Q4_OK) return st;
+    if (!aligned(W->tiled, 16) || !aligned(X, 16) || !aligned(Y, 4)) return Q4_ERR_MISALIGNED;
+    const size_t need = prefill_ws(W->K, M);
+    if (!ws || ws_bytes < need) return Q4_ERR_WORKSPACE;
+    if (!aligned(ws, 16)) return Q4_ERR_MISALIGNED;
+    if (fault_injected()) return Q4_ERR_CUDA;
+    int dev = 0;
+    if (device_sm_count(&dev) <= 0) return Q4_ERR_CUDA;
+    const Knobs k = knobs();
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const size_t stride = prep_bytes(W->K, 8);
+    const size_t G = static_cast<size_t>(W->K / 128);
+    const int64_t nblk = (M + 7) / 8;
+    unsigned char* base = static_cast<unsigned char*>(ws);
+    // activations: one prep job per token block of 8 (the last one may hold fewer tokens)
+    for (int64_t b0 = 0; b0 < nblk;) {
+        const int64_t full_end = M / 8;  // blocks [0, full_end) hold 8 tokens
+        const bool partial = b0 >= full_end;
+        int64_t b1 = partial ? b0 + 1 : (b0 + kMaxMats < full_end ? b0 + kMaxMats : full_end);
+        PrepParams pp;
+        std::memset(&pp, 0, sizeof pp);
+        pp.n = static_cast<int>(b1 - b0);
+        pp.B = partial ? static_cast<int>(M - 8 * b0) : 8;
+        for (int64_t b = b0; b < b1; ++b) {
+            PrepJob& j = pp.j[b - b0];
+            unsigned char* w = base + static_cast<size_t>(b) * stride;
+            j.x = X + static_cast<size_t>(b) * 8 * W->K;
+            j.K = static_cast<int>(W->K);
+            j.xf = reinterpret_cast<uint2*>(w);
+            j.S = reinterpret_cast<float*>(w + G * 256 * 8);
+            j.fac = j.S + G * 8;
+        }
+        st = launch(q4_xprep_kernel<8>, dev, static_cast<unsigned>(pp.n), 256u, 0, cs, k.pdl, pp);
+        if (st != Q4_OK) return st;
+        b0 = b1;
+    }
+    PrefillParams fp;
+    std::memset(&fp, 0, sizeof fp);
+    fp.tiled = static_cast<const uint8_t*>(W->tiled);
+    fp.prep = base;
+    fp.prep_stride = stride;
+    fp.y = Y;
+    fp.N = static_cast<int>(W->N);
+    fp.K = static_cast<int>(W->K);
+    fp.M = static_cast<int>(M);
+    // CTA tile: 8 row tiles x 8 token blocks; 4 x 4 when that would leave SMs without a CTA (small
+    // matrices with short prompts)
+    const int64_t T = (W->N + 15) / 16;
+    const int sms = device_sm_count(nullptr);
+    const bool small = ((T + 7) / 8) * ((nblk + 7) / 8) < sms;
+    const int pw = small ? 4 : 8, ptb = small ? 4 : 8;
+    const dim3 grid(static_cast<unsigned>((T + pw - 1) / pw), static_cast<unsigned>((nblk + ptb - 1) / ptb));
+    if (grid.y > 65535) return Q4_ERR_UNSUPPORTED_SHAPE;
+    using PfFn = void (*)(PrefillParams);
+    const PfFn pf = small ? q4_prefill_kernel<4, 4> : q4_prefill_kernel<8, 8>;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(pw * 32);
+    cfg.stream = cs;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = k.pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pf, fp) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ the int8 head
