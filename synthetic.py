@@ -94,3 +94,26 @@ def decode_step_matrix(layer: int, proj: int, B: int = 1, base: int = 0):
 def random_shape_problem(N: int, K: int, B: int, seed: int, outliers: bool = False):
     w, rng = weights(N, K, seed, outliers)
     return w, activations(B, K, rng)
+
+
+# ------------------------------------------------------------------ attention over a KV cache
+# "Step 6: flash-decoding for long clips": one decode step's attention over a cache of about
+# 2,000 positions, with 4 query heads per KV head.  The head layout is read from the shapes
+# above: the o-projection's input of 3072 = 24 query heads x 128, so 6 KV heads.
+Q_HEADS, KV_HEADS, HEAD_DIM = 24, 6, 128
+CACHE_LEN = 2000
+
+
+def attention_problem(B: int, Hq: int, Hkv: int, D: int, Lmax: int, lengths, seed: int,
+                      q_std: float = 1.0):
+    """(Q [B, Hq, D], K [B, Hkv, Lmax, D], V [B, Hkv, Lmax, D] as bf16 bits, lengths int32 [B]).
+
+    Recipe: rng = default_rng(seed); Q = N(0, 1) * q_std, then K = N(0, 1), then V = N(0, 1),
+    each drawn as float32 in that order and rounded to bf16 (nearest-even).  q_std sets how
+    peaked the softmax is (scores have standard deviation q_std * sqrt(D) * scale)."""
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Hq, D), dtype=np.float32) * np.float32(q_std)
+    k = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)
+    v = rng.standard_normal((B, Hkv, Lmax, D), dtype=np.float32)
+    lens = np.broadcast_to(np.asarray(lengths, np.int32), (B,)).copy()
+    return f32_to_bf16_bits(q), f32_to_bf16_bits(k), f32_to_bf16_bits(v), lens
