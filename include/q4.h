@@ -372,6 +372,43 @@ q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float* Y, int32_
                   size_t ws_bytes, void* stream);
 
 /*
+ * q4_flash_decode -- one decode step of grouped-query attention over a KV
+ * cache, split over chunks of the cache (the rumik-oss-1 write-up, "Step 6:
+ * flash-decoding for long clips": the cache of each KV head split into
+ * chunks, the query heads that share a KV head computed in one tensor-core
+ * tile, the chunks' partial results merged by a second kernel).  For every
+ * sequence b and query head h, with g = n_q_heads / n_kv_heads:
+ *     O[b,h,:] = sum_{p < len_b} softmax_p(scale * <Q[b,h,:], K[b,h/g,p,:]>) V[b,h/g,p,:]
+ * (query head h reads KV head h / g).  fp32 softmax and accumulation; the
+ * weights enter the tensor cores as bf16 hi + lo parts (relative error below
+ * 2^-18).
+ *   Q        device bf16 bits [B, n_q_heads, head_dim], 16-byte aligned.
+ *   K_cache, V_cache  device bf16 bits [B, n_kv_heads, max_len, head_dim], 16-byte aligned
+ *            (every KV head's positions contiguous).
+ *   lengths  device int32 [B]: len_b = lengths[b] clamped to 0..max_len; only
+ *            positions 0..len_b-1 are read.  len_b = 0 gives O[b] = 0.
+ *   head_dim 64 or 128;  1 <= n_q_heads / n_kv_heads <= 16 (a whole multiple);
+ *   B, n_kv_heads 1..65535;  1 <= max_len <= 2^30;  scale finite.
+ *   n_chunks chunks per KV head, 1..4096, or 0 for the default of about two
+ *            CTAs per SM for one sequence (q4_flash_decode_chunks reports it).
+ *            The chunk length is ceil(len_b / chunks) rounded up to 16, so a
+ *            sequence's result does not depend on B or on the other sequences.
+ *   O        device fp32 [B, n_q_heads, head_dim], 4-byte aligned.
+ *   ws       device workspace, 16-byte aligned, of ws_bytes >=
+ *            q4_flash_decode_workspace_bytes(...) (no initial content needed).
+ * Two kernels on `stream` (chained by programmatic dependent launch); nothing
+ * allocated.  Q4_ERR_INVALID_ARG for null pointers or out-of-range B, heads,
+ * group, chunks, max_len or scale; Q4_ERR_UNSUPPORTED_SHAPE for another
+ * head_dim; Q4_ERR_MISALIGNED; Q4_ERR_WORKSPACE if ws_bytes is too small.
+ */
+int q4_flash_decode_chunks(int n_kv_heads, int n_chunks);
+size_t q4_flash_decode_workspace_bytes(int B, int n_q_heads, int n_kv_heads, int head_dim, int n_chunks);
+q4_status q4_flash_decode(const uint16_t* Q, const uint16_t* K_cache, const uint16_t* V_cache,
+                          const int32_t* lengths, int B, int n_q_heads, int n_kv_heads, int head_dim,
+                          int64_t max_len, float scale, int n_chunks, float* O, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/*
  * q4_device_status -- wait for `stream`, then read and clear the device error
  * word.  Every wait inside the kernels is bounded; one that gives up sets the
  * word and the kernel carries on to its end (its outputs are then invalid).

@@ -27,7 +27,7 @@ __all__ = ["GROUP", "MAX_B", "Q4Error", "QuantizedMatrix", "Workspace", "pack_ho
            "workspace_bytes", "decode_step_workspace_bytes", "tiled_bytes", "gemv", "gemm_skinny", "decode_step",
            "argmax", "device_status", "DecodeStepGraph", "step_workspace_bytes", "step_prepare", "step_stream",
            "gemm_skinny_noalloc", "pack_int8_host", "Int8Head", "sample_topk", "gemm_prefill",
-           "header_functions", "lib"]
+           "flash_decode", "flash_decode_workspace", "header_functions", "lib"]
 
 
 def _stream_ptr(stream) -> int:
@@ -353,6 +353,41 @@ def sample_topk(Y: torch.Tensor, k: int, inv_temperature: float, noise: torch.Te
     check(lib.q4_sample_topk(_ptr(Y2), B, N, int(k), float(inv_temperature), _ptr(noise), _ptr(token),
                              _ptr(topk) if topk is not None else None, _stream_ptr(stream)), "q4_sample_topk")
     return (token, topk) if return_topk else token
+
+
+def flash_decode_workspace(B: int, n_q_heads: int, n_kv_heads: int, head_dim: int, n_chunks: int = 0,
+                           device="cuda") -> Workspace:
+    """Workspace for flash_decode with these sizes (q4_flash_decode_workspace_bytes)."""
+    n = int(lib.q4_flash_decode_workspace_bytes(B, n_q_heads, n_kv_heads, head_dim, n_chunks))
+    if n == 0:
+        raise Q4Error(1, "q4_flash_decode_workspace_bytes")
+    return Workspace(n, device)
+
+
+def flash_decode(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, lengths: torch.Tensor,
+                 O: torch.Tensor | None = None, scale: float | None = None, n_chunks: int = 0,
+                 workspace: Workspace | None = None, stream=None) -> torch.Tensor:
+    """One decode step of grouped-query attention over a KV cache (q4_flash_decode).
+
+    Q bf16 [B, Hq, D]; K, V bf16 [B, Hkv, Lmax, D]; lengths int32 [B] on the device; returns
+    O fp32 [B, Hq, D].  scale defaults to 1/sqrt(D)."""
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous torch.bfloat16 CUDA tensor")
+    if lengths.dtype != torch.int32 or not lengths.is_contiguous():
+        raise TypeError("lengths must be a contiguous int32 CUDA tensor")
+    B, Hq, D = Q.shape
+    _, Hkv, Lmax, _ = K.shape
+    if tuple(K.shape) != (B, Hkv, Lmax, D) or tuple(V.shape) != tuple(K.shape):
+        raise ValueError("K and V must be [B, Hkv, Lmax, D] matching Q [B, Hq, D]")
+    if O is None:
+        O = torch.empty((B, Hq, D), dtype=torch.float32, device=Q.device)
+    if workspace is None:
+        workspace = flash_decode_workspace(B, Hq, Hkv, D, n_chunks, Q.device)
+    sc = float(scale) if scale is not None else 1.0 / float(D) ** 0.5
+    check(lib.q4_flash_decode(_ptr(Q), _ptr(K), _ptr(V), _ptr(lengths), B, Hq, Hkv, D, Lmax, sc, int(n_chunks),
+                              _ptr(O), *_ws_args(workspace), _stream_ptr(stream)), "q4_flash_decode")
+    return O
 
 
 class DecodeStepGraph:

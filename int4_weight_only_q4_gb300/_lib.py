@@ -102,6 +102,13 @@ lib.q4_prefill_workspace_bytes.argtypes = [c_i64, c_i64]
 lib.q4_prefill_workspace_bytes.restype = ctypes.c_size_t
 lib.q4_gemm_prefill.argtypes = [ctypes.POINTER(q4_matrix), c_vp, c_i64, c_vp, c_vp, ctypes.c_size_t, c_vp]
 lib.q4_gemm_prefill.restype = ctypes.c_int
+lib.q4_flash_decode_chunks.argtypes = [ctypes.c_int, ctypes.c_int]
+lib.q4_flash_decode_chunks.restype = ctypes.c_int
+lib.q4_flash_decode_workspace_bytes.argtypes = [ctypes.c_int] * 5
+lib.q4_flash_decode_workspace_bytes.restype = ctypes.c_size_t
+lib.q4_flash_decode.argtypes = [c_vp, c_vp, c_vp, c_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                c_i64, ctypes.c_float, ctypes.c_int, c_vp, c_vp, ctypes.c_size_t, c_vp]
+lib.q4_flash_decode.restype = ctypes.c_int
 lib.q4_status_string.argtypes = [ctypes.c_int]
 lib.q4_status_string.restype = ctypes.c_char_p
 

@@ -65,6 +65,7 @@
 #include <vector>
 
 #include "q4.h"
+#include "q4_common.cuh"
 
 namespace {
 
@@ -105,24 +106,6 @@ __device__ __forceinline__ uint32_t ld_nc_u16(const uint16_t* p) {
     return v;
 }
 
-__device__ __forceinline__ void mma_bf16_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// d = A * B (the accumulator input is zero)
-__device__ __forceinline__ void mma_bf16_m16n8k16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                                     uint32_t a3, uint32_t b0, uint32_t b1) {
-    const float z = 0.f;
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
-}
-
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
@@ -130,27 +113,12 @@ __device__ __forceinline__ float half_bits_to_f32(uint32_t h) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
 }
 
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Ask L2 to fetch [p, p + bytes) from DRAM (bytes: multiple of 16, p: 16-byte aligned).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// 16-byte asynchronous copy global -> shared (through L2 only) and its group bookkeeping.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 // wait_group with a run-time count n in [0, N]
 template <int N>
 __device__ __forceinline__ void cp_async_wait_upto(int n) {
@@ -242,39 +210,15 @@ __device__ __forceinline__ size_t xfrag_index(int gl, int i, int p) {
     return (static_cast<size_t>(gl) * 8 + i * 2 + p) * (4 * BT);
 }
 
-// qa/qb: this lane's 32 codes (16 bytes) of tile rows q and q+8, columns 32t..32t+31 of the group.
-// xg: the group's staged activations.  c: rows (q, q, q+8, q+8) x batch columns (2t, 2t+1, 2t,
-// 2t+1) of sum_k code * x * 2^(a-133).
-// Loads of data the previous kernel in the stream wrote (activations, their prepared copy,
-// logits): ordinary coherent loads, in volatile asm so that they stay after the
-// griddepcontrol.wait that makes that data visible.  (A non-coherent ld.global.nc is only
-// valid for data that is read-only for the whole life of the kernel, and the compiler may move
-// it above the wait.)
-__device__ __forceinline__ uint2 ld_dep_u2(const void* p) {
-    uint2 r;
-    asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p) : "memory");
-    return r;
-}
-__device__ __forceinline__ uint4 ld_dep_u4(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p)
-                 : "memory");
-    return r;
-}
-__device__ __forceinline__ float ld_dep_f32(const float* p) {
-    float r;
-    asm volatile("ld.global.f32 %0, [%1];" : "=f"(r) : "l"(p) : "memory");
-    return r;
-}
-
 template <bool GLOBAL>
 __device__ __forceinline__ uint2 ld_x(const uint2* p) {
     if constexpr (GLOBAL) return ld_dep_u2(p);
     return *p;
 }
 
+// qa/qb: this lane's 32 codes (16 bytes) of tile rows q and q+8, columns 32t..32t+31 of the group.
+// xg: the group's staged activations.  c: rows (q, q, q+8, q+8) x batch columns (2t, 2t+1, 2t,
+// 2t+1) of sum_k code * x * 2^(a-133).
 template <bool MMA, int BT, bool XG = false>
 __device__ __forceinline__ void group_dot(const uint4& qa, const uint4& qb, const uint2* xg, int lane, int B,
                                           float (&c)[4]) {
@@ -2387,10 +2331,7 @@ q4_status check_io(const uint16_t* X, int B, const float* Y) {
     return Q4_OK;
 }
 
-bool fault_injected() {
-    const char* v = std::getenv("Q4_FAULT_INJECT");
-    return v && std::strcmp(v, "launch") == 0;
-}
+bool fault_injected() { return q4i_fault_injected(); }
 
 template <typename Fn>
 bool smem_attr_set(Fn fn, int dev) {
@@ -2812,6 +2753,13 @@ size_t workspace_for(const int64_t* N, const int64_t* K, int n, int B, bool inde
 }
 
 }  // namespace
+
+int q4i_sm_count(int* dev_out) { return device_sm_count(dev_out); }
+
+bool q4i_fault_injected() {
+    const char* v = std::getenv("Q4_FAULT_INJECT");
+    return v && std::strcmp(v, "launch") == 0;
+}
 
 // ------------------------------------------------------------------ C ABI
 extern "C" size_t q4_tiled_bytes(int64_t N, int64_t K) {

@@ -90,3 +90,35 @@ def test_sampler_argument_checks_before_any_launch():
     assert L.q4_sample_topk(None, 1, 100, 5, 1.0, f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
     assert L.q4_sample_topk(f, 0, 100, 5, 1.0, f, f, None, None) == _lib.Q4_ERR_INVALID_ARG
     assert L.q4_sample_topk(f + 2, 1, 100, 5, 1.0, f, f, None, None) == _lib.Q4_ERR_MISALIGNED
+
+
+def test_flash_decode_argument_checks_before_any_launch():
+    L = _lib.lib
+    p = 1 << 20                                      # never dereferenced: every call fails its checks
+    ws = L.q4_flash_decode_workspace_bytes(2, 24, 6, 128, 16)
+    assert ws == 2 * 24 * 16 * 128 * 4 + 2 * 24 * 16 * 2 * 4
+    assert L.q4_flash_decode_chunks(6, 16) == 16
+    assert L.q4_flash_decode_workspace_bytes(2, 24, 5, 128, 16) == 0       # 24 not a multiple of 5
+    assert L.q4_flash_decode_workspace_bytes(1, 34, 2, 128, 1) == 0        # group 17 > 16
+    assert L.q4_flash_decode_workspace_bytes(1, 8, 2, 96, 1) == 0          # head_dim 96
+
+    def call(Q=p, K=p, V=p, lens=p, B=2, Hq=24, Hkv=6, D=128, Lmax=2000, scale=0.088, C=16, O=p, w=p, nb=ws):
+        return L.q4_flash_decode(Q, K, V, lens, B, Hq, Hkv, D, Lmax, scale, C, O, w, nb, None)
+
+    E = _lib
+    assert call(Q=None) == E.Q4_ERR_INVALID_ARG
+    assert call(lens=None) == E.Q4_ERR_INVALID_ARG
+    assert call(w=None) == E.Q4_ERR_INVALID_ARG
+    assert call(B=0) == E.Q4_ERR_INVALID_ARG
+    assert call(Hq=25) == E.Q4_ERR_INVALID_ARG
+    assert call(Hq=102, Hkv=6) == E.Q4_ERR_INVALID_ARG                     # group 17
+    assert call(C=-1) == E.Q4_ERR_INVALID_ARG and call(C=4097) == E.Q4_ERR_INVALID_ARG
+    assert call(Lmax=0) == E.Q4_ERR_INVALID_ARG and call(Lmax=(1 << 30) + 1) == E.Q4_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == E.Q4_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == E.Q4_ERR_INVALID_ARG
+    assert call(D=80) == E.Q4_ERR_UNSUPPORTED_SHAPE
+    assert call(Q=p + 8) == E.Q4_ERR_MISALIGNED
+    assert call(K=p + 4) == E.Q4_ERR_MISALIGNED
+    assert call(O=p + 2) == E.Q4_ERR_MISALIGNED
+    assert call(lens=p + 1) == E.Q4_ERR_MISALIGNED
+    assert call(nb=ws - 1) == E.Q4_ERR_WORKSPACE
