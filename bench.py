@@ -377,6 +377,7 @@ def run_ours(args):
     head8 = int8_head(q4, torch, dev, args)
     samp = sampler_bench(q4, torch, dev, args)
     prefill = prefill_bench(q4, torch, mats, dev, args)
+    attn = attention_bench(q4, torch, dev, args)
 
     # end to end through the public API with pinned host buffers
     e2e = end_to_end(q4, torch, g1, xs1, dev, max(10, args.steps // 20), barrier)
@@ -393,6 +394,7 @@ def run_ours(args):
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "roofline": roof, "fused_projection_sustained": fused_sus, "fused_gemv_single_call": fused_single,
         "int8_head_65536x3072": head8, "sampler_topk_gumbel": samp, "prefill_gemm": prefill,
+        "flash_decoding_attention": attn,
         "gen_seconds": round(gen_s, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -626,6 +628,57 @@ def prefill_bench(q4, torch, mats, dev, args):
     return out
 
 
+def attention_bench(q4, torch, dev, args):
+    """Flash-decoding attention (q4_flash_decode): 24 query heads sharing 6 KV heads, head_dim 128.
+    The page's case -- batch 1 over a 2,000-position cache -- as one call per layer for 36 layers
+    (36 distinct caches, 221 MB, so nothing stays in L2) in one CUDA graph; and a long cache,
+    batch 8 over 8,192 positions (2 layers, 403 MB).  Microseconds per call and GB/s of
+    algorithmic bytes (keys, values, queries, outputs)."""
+    Hq, Hkv, D = 24, 6, 128
+    peak, src = measured_peak_gbs()
+    out = {"heads": f"{Hq} query / {Hkv} KV heads, head_dim {D}", "chunks_per_kv_head": int(q4.lib.q4_flash_decode_chunks(Hkv, 0))}
+    for name, B, L, layers, C in (("page_b1_2000", 1, 2000, 36, 0), ("page_b1_2000_16chunks", 1, 2000, 36, 16),
+                                  ("long_b8_8192", 8, 8192, 2, 0)):
+        g = torch.Generator(device=dev).manual_seed(args.seed)
+        Qs = [torch.randn((B, Hq, D), device=dev, generator=g).to(torch.bfloat16) for _ in range(layers)]
+        Ks = [torch.randn((B, Hkv, L, D), device=dev, generator=g).to(torch.bfloat16) for _ in range(layers)]
+        Vs = [torch.randn((B, Hkv, L, D), device=dev, generator=g).to(torch.bfloat16) for _ in range(layers)]
+        lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+        O = torch.empty((B, Hq, D), device=dev)
+        ws = q4.flash_decode_workspace(B, Hq, Hkv, D, C, dev)
+        reps = max(1, 36 // layers)
+        side = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(side):
+            for i in range(layers):
+                q4.flash_decode(Qs[i], Ks[i], Vs[i], lens, O, n_chunks=C, workspace=ws, stream=side)
+            side.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(reps):
+                    for i in range(layers):
+                        q4.flash_decode(Qs[i], Ks[i], Vs[i], lens, O, n_chunks=C, workspace=ws, stream=side)
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
+        n = max(10, args.steps // 100)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / (n * reps * layers)
+        nbytes = 2 * B * Hkv * L * D * 2 + B * Hq * D * (2 + 4)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"us_per_call": round(us, 2), "GB/s": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+                     "algorithmic_bytes": nbytes}
+        del Qs, Ks, Vs, graph
+    out["kernel"] = "q4_flash_split_kernel<128, 3> + q4_flash_combine_kernel<128> (per call)"
+    out["bound"] = "hbm"
+    out["peak_source"] = src
+    return out
+
+
 def end_to_end(q4, torch, g, xs, dev, steps, barrier):
     """Per step through the public API: the step's activations host->device (one pinned buffer laid
     out like the graph's activation buffer), graph replay, the step's result (the head's argmax
@@ -684,7 +737,8 @@ def run_profile_case(args) -> int:
 def run_profile_small(args) -> int:
     """Small cases for ncu: `--profile-head8` one int8-head call (65,536 x 3072, seeded random codes on
     the device, B = --profile-batch, logits + argmax) after two warm-up calls; `--profile-sampler`
-    one top-k (k = 50) Gumbel-max sampling call over 65,536 logits after two warm-up calls."""
+    one top-k (k = 50) Gumbel-max sampling call over 65,536 logits after two warm-up calls;
+    `--profile-attn` three flash-decoding calls, batch --profile-batch over an 8,192-position cache."""
     import torch
     import int4_weight_only_q4_gb300 as q4
     dev = torch.device("cuda", 0)
@@ -699,15 +753,24 @@ def run_profile_small(args) -> int:
         X = torch.randn((B, K), device=dev, generator=gen).to(torch.bfloat16)
         for _ in range(3):
             Y, idx = H(X)
-    else:
+    elif args.profile_sampler:
         Y = torch.randn((B, N), device=dev, generator=gen) * 3
         noise = torch.zeros((B, 50), device=dev)
         for _ in range(3):
             idx = q4.sample_topk(Y, 50, 1.0, noise)
+    else:  # attention: batch --profile-batch over an 8,192-position cache (24 / 6 heads, head_dim 128)
+        L = 8192
+        Q = torch.randn((B, 24, 128), device=dev, generator=gen).to(torch.bfloat16)
+        Kc = torch.randn((B, 6, L, 128), device=dev, generator=gen).to(torch.bfloat16)
+        Vc = torch.randn((B, 6, L, 128), device=dev, generator=gen).to(torch.bfloat16)
+        lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            O = q4.flash_decode(Q, Kc, Vc, lens)
+        idx = [float(O.abs().mean())]
     torch.cuda.synchronize()
     q4.device_status()
-    print(json.dumps({"profile_case": "int8 head" if args.profile_head8 else "sampler", "B": B,
-                      "idx": idx.cpu().tolist()}))
+    case = "int8 head" if args.profile_head8 else "sampler" if args.profile_sampler else "attention"
+    print(json.dumps({"profile_case": case, "B": B, "idx": idx if isinstance(idx, list) else idx.cpu().tolist()}))
     return 0
 
 
@@ -725,10 +788,11 @@ def main():
     ap.add_argument("--profile-batch", type=int, default=1)
     ap.add_argument("--profile-head8", action="store_true", help="run only a small int8-head case for ncu")
     ap.add_argument("--profile-sampler", action="store_true", help="run only a small sampler case for ncu")
+    ap.add_argument("--profile-attn", action="store_true", help="run only a flash-decoding attention case for ncu")
     args = ap.parse_args()
     if args.profile_step > 0:
         return run_profile_case(args)
-    if args.profile_head8 or args.profile_sampler:
+    if args.profile_head8 or args.profile_sampler or args.profile_attn:
         return run_profile_small(args)
     if args.impl == "reference":
         return run_reference(args)

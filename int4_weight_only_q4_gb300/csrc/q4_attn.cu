@@ -16,9 +16,11 @@
 // the workspace when the chunk ends.  A chunk's arithmetic is the same whichever warp runs it,
 // so the host may choose the number of CTAs per KV head from B and the SM count without
 // changing a bit of any sequence's result.  A warp streams the 16-position tiles of its chunks
-// -- keys and values, every byte once -- through its own ring of shared-memory slots with 16-byte
-// cp.async copies, two tiles ahead, across chunk boundaries; each lane reads back only the
-// pieces it copied.  Per tile it
+// -- keys and values, every byte once -- through its own ring of three shared-memory slots, two
+// tiles ahead, across chunk boundaries: each lane issues one bulk copy (the TMA engine) of one
+// key or value row into a padded slot row, and an mbarrier per slot counts the bytes in.  (A
+// second fill, 16-byte cp.async copies that each lane reads back itself, streams measurably
+// slower and is kept as an option.)  Per tile it
 //   * computes the 16 x 16 score tile S = Q K^T with mma.m16n8k16 (rows: the g query heads of
 //     this KV head, padded to 16 with zero queries; columns: positions), bf16 in, fp32 out;
 //   * updates a running softmax in base 2 (u = s * scale * log2 e; running maximum m and sum l
@@ -43,8 +45,10 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <map>
 #include <mutex>
 #include <set>
+#include <tuple>
 #include <utility>
 
 #include "q4.h"
@@ -72,6 +76,21 @@ struct FdParams {
     float c;                  // scale * log2(e)
     int Hkv, g, C, min_chunk;
 };
+
+constexpr uint32_t kFdWaitLimit = 1u << 22;  // mbarrier polls before a wait gives up
+
+__device__ unsigned int g_fd_device_error;  // set when a bounded wait gives up
+
+// Per-warp ring slot of one 16-position tile.  Bulk slots pad the rows (keys to 2D + 64 bytes,
+// values to 2D + 16) so that the lanes' 16-byte fragment reads fall in distinct bank groups.
+template <int D, bool BULK>
+struct FdSlot {
+    static constexpr int kKeyStride = 2 * D + 64;
+    static constexpr int kValueStride = 2 * D + 16;
+    static constexpr int kBytes = BULK ? 16 * (kKeyStride + kValueStride) : 16 * 2 * D * 2;
+};
+
+__device__ __forceinline__ uint4 lds_u4(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
 
 // attended positions of sequence b (clamped to 0..Lmax), its chunk length and chunk count
 __device__ __forceinline__ void fd_chunking(const FdParams& p, int b, int& len, int& cs, int& used) {
@@ -112,14 +131,18 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
     lo = bf16x2_bits(a - __low2float(h), b - __high2float(h));
 }
 
-template <int D, int S>
+template <int D, int S, bool BULK>
 __global__ void __launch_bounds__(kFdWarps * 32) q4_flash_split_kernel(const __grid_constant__ FdParams p) {
     constexpr int KJ = D / 32;  // 16-byte key pieces per position per lane (4 lanes share a key)
     constexpr int VJ = D / 64;  // 16-byte value pieces per position per lane (8 lanes share a row)
     constexpr int NP = D / 8;   // pieces per lane per tile: 2 KJ keys + 4 VJ values
     constexpr int NT = D / 8;   // output column tiles of P V
     constexpr int KS = D / 16;  // k-steps of Q K^T
-    extern __shared__ __align__(16) unsigned char fd_smem_raw[];  // [warp][slot][piece][lane]
+    constexpr int KSTR = FdSlot<D, BULK>::kKeyStride, VSTR = FdSlot<D, BULK>::kValueStride;
+    constexpr int SLOT = FdSlot<D, BULK>::kBytes;
+    // [warp][slot]: cp.async slots hold [piece][lane] (each lane reads back only what it copied);
+    // bulk slots hold 16 padded key rows then 16 padded value rows, then the slots' mbarriers
+    extern __shared__ __align__(16) unsigned char fd_smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int q = lane >> 2, t = lane & 3;
     const int kvh = blockIdx.y, b = blockIdx.z;
@@ -137,6 +160,16 @@ __global__ void __launch_bounds__(kFdWarps * 32) q4_flash_split_kernel(const __g
     const uint16_t* Kh = p.K + head * p.Lmax * D;
     const uint16_t* Vh = p.V + head * p.Lmax * D;
     uint4* ring = reinterpret_cast<uint4*>(fd_smem_raw) + static_cast<size_t>(warp) * S * NP * 32 + lane;
+    unsigned char* wslots = fd_smem_raw + static_cast<size_t>(warp) * S * SLOT;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(fd_smem_raw + static_cast<size_t>(kFdWarps) * S * SLOT) + warp * S;
+    if constexpr (BULK) {
+        if (lane == 0) {
+#pragma unroll
+            for (int sl = 0; sl < S; ++sl) mbar_init(&bars[sl], 1);
+            fence_barrier_init();
+        }
+        __syncwarp();
+    }
 
     // The warp's tiles in order: chunk w0's, then chunk w0 + nw's, ...  Copy the next one into
     // the next slot: keys of positions base + 8h + q (h = 0, 1), dims 32j + 8t .. +7; values of
@@ -144,9 +177,21 @@ __global__ void __launch_bounds__(kFdWarps * 32) q4_flash_split_kernel(const __g
     // copy its last row (finite data; their weight is exactly 0).  One commit group per call.
     int ic = w0, it = 0, islot = 0;
     auto issue_next = [&]() {
+        if constexpr (BULK) __syncwarp();  // every lane has read the slot being refilled
         if (ic < used) {
             const int s0 = ic * cs, e0 = min(len, s0 + cs);
             const int base = s0 + 16 * it;
+            if constexpr (BULK) {
+                // lane r < 16: key row base + r; lane 16 + r: value row base + r (one bulk copy each)
+                unsigned char* dst = wslots + static_cast<size_t>(islot) * SLOT;
+                if (lane == 0) mbar_arrive_expect_tx(&bars[islot], 32 * 2 * D);
+                __syncwarp();
+                const int r = lane & 15, pos = min(base + r, e0 - 1);
+                if (lane < 16)
+                    bulk_g2s(dst + r * KSTR, Kh + static_cast<size_t>(pos) * D, 2 * D, &bars[islot]);
+                else
+                    bulk_g2s(dst + 16 * KSTR + r * VSTR, Vh + static_cast<size_t>(pos) * D, 2 * D, &bars[islot]);
+            } else {
             uint4* dst = ring + static_cast<size_t>(islot) * NP * 32;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -162,6 +207,7 @@ __global__ void __launch_bounds__(kFdWarps * 32) q4_flash_split_kernel(const __g
                 for (int j = 0; j < VJ; ++j)
                     cp_async16(dst + (2 * KJ + i * VJ + j) * 32, Vh + static_cast<size_t>(pos) * D + 64 * j + 8 * q);
             }
+            }
             if (base + 16 >= e0) {  // that was the chunk's last tile
                 ic += nw;
                 it = 0;
@@ -169,7 +215,7 @@ __global__ void __launch_bounds__(kFdWarps * 32) q4_flash_split_kernel(const __g
                 ++it;
             }
         }
-        cp_async_commit();
+        if constexpr (!BULK) cp_async_commit();
         islot = islot == S - 1 ? 0 : islot + 1;
     };
 #pragma unroll
@@ -191,8 +237,10 @@ __global__ void __launch_bounds__(kFdWarps * 32) q4_flash_split_kernel(const __g
         qa[m][3] = r1.y;
     }
 
-    int rs = 0;  // ring slot of the tile being computed
-    for (int cc = w0; cc < used; cc += nw) {
+    int rs = 0;           // ring slot of the tile being computed
+    uint32_t phase = 0;   // bulk: parity of that slot's current use (flips after slot S-1)
+    bool ok = true;
+    for (int cc = w0; cc < used && ok; cc += nw) {
         const int s0 = cc * cs, e0 = min(len, s0 + cs);
         float acc[NT][4];
 #pragma unroll
@@ -201,19 +249,42 @@ __global__ void __launch_bounds__(kFdWarps * 32) q4_flash_split_kernel(const __g
         float lsum[2] = {0.f, 0.f};              // this lane's share of the row sums
 
         for (int base = s0; base < e0; base += 16) {
-            cp_async_wait<S - 2>();  // this lane's copies of the tile have landed
-            issue_next();
-            const uint4* src = ring + static_cast<size_t>(rs) * NP * 32;
-            rs = rs == S - 1 ? 0 : rs + 1;
             uint4 kr[2][KJ], vr[4][VJ];
+            if constexpr (BULK) {
+                if (!mbar_wait(&bars[rs], phase, kFdWaitLimit)) {  // the tile's 32 rows have landed
+                    ok = false;
+                    break;
+                }
+                const unsigned char* src = wslots + static_cast<size_t>(rs) * SLOT;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int j = 0; j < KJ; ++j) kr[h][j] = src[(h * KJ + j) * 32];
+                    for (int j = 0; j < KJ; ++j) kr[h][j] = lds_u4(src + (8 * h + q) * KSTR + 64 * j + 16 * t);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < VJ; ++j) vr[i][j] = src[(2 * KJ + i * VJ + j) * 32];
+                    for (int j = 0; j < VJ; ++j)
+                        vr[i][j] = lds_u4(src + 16 * KSTR + (8 * (i >> 1) + 2 * t + (i & 1)) * VSTR + 128 * j + 16 * q);
+                issue_next();
+            } else {
+                cp_async_wait<S - 2>();  // this lane's copies of the tile have landed
+                issue_next();
+                const uint4* src = ring + static_cast<size_t>(rs) * NP * 32;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int j = 0; j < KJ; ++j) kr[h][j] = src[(h * KJ + j) * 32];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < VJ; ++j) vr[i][j] = src[(2 * KJ + i * VJ + j) * 32];
+            }
+            if (rs == S - 1) {
+                rs = 0;
+                phase ^= 1u;
+            } else {
+                ++rs;
+            }
 
             // S: s[h][0..1] = row q, columns 2t, 2t+1 of half h; s[h][2..3] = row q+8.  Even and
             // odd k-steps go to separate accumulators (four independent chains), added at the end.
@@ -318,7 +389,20 @@ __global__ void __launch_bounds__(kFdWarps * 32) q4_flash_split_kernel(const __g
             }
         }
     }
-    cp_async_wait<0>();
+    if constexpr (BULK) {
+        if (!ok) {
+            // a copy did not land within the limit: report it, give every slot a bounded last wait
+            // so that no copy is left writing into this block's shared memory, and stop
+            if (lane == 0) atomicOr(&g_fd_device_error, 1u);
+#pragma unroll
+            for (int sl = 0; sl < S; ++sl) {
+                mbar_wait(&bars[sl], 0u, kFdWaitLimit);
+                mbar_wait(&bars[sl], 1u, kFdWaitLimit);
+            }
+        }
+    } else {
+        cp_async_wait<0>();
+    }
 }
 
 // fixed-order block reductions over kFdCombineThreads threads (the same tree for every call)
@@ -446,6 +530,39 @@ bool smem_limit_raised(void (*fn)(FdParams), size_t bytes) {
 
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
+// CTAs of the split kernel resident per SM with this much dynamic shared memory (cached per
+// kernel, size and device; 0 on error)
+int resident_ctas(void (*fn)(FdParams), size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, size_t, int>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_tuple(reinterpret_cast<const void*>(fn), smem, dev);
+    const auto hit = cache.find(key);
+    if (hit != cache.end()) return hit->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kFdWarps * 32, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[key] = n;
+    return n;
+}
+
+// how the split kernel fills its ring: one bulk copy per row (default) or per-lane 16-byte
+// cp.async (Q4_FD_BULK=0); both give the same bits
+bool fd_bulk() {
+    const char* v = std::getenv("Q4_FD_BULK");
+    return !(v && *v && std::atoi(v) == 0);
+}
+
+// ring slots per warp of the cp.async fill (Q4_FD_STAGES = 2 or 3)
+int fd_stages() {
+    const char* v = std::getenv("Q4_FD_STAGES");
+    return v && std::atoi(v) == 2 ? 2 : kFdStages;
+}
+
 int fd_chunks(int n_kv_heads, int n_chunks, int sms) {
     if (n_chunks > 0) return n_chunks;
     // about eight chunks per SM for one sequence (chunks are still at least kFdMinChunk long)
@@ -467,6 +584,15 @@ q4_status fd_check(int B, int Hq, int Hkv, int D, int n_chunks) {
 }
 
 }  // namespace
+
+int q4i_attn_take_error() {
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fd_device_error, sizeof v) != cudaSuccess) return -1;
+    if (v == 0) return 0;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_fd_device_error, &zero, sizeof zero) != cudaSuccess) return -1;
+    return 1;
+}
 
 // ------------------------------------------------------------------ C ABI
 extern "C" int q4_flash_decode_chunks(int n_kv_heads, int n_chunks) {
@@ -526,11 +652,6 @@ extern "C" q4_status q4_flash_decode(const uint16_t* Q, const uint16_t* K_cache,
     p.C = C;
     p.min_chunk = kFdMinChunk;
 
-    // CTAs per (sequence, KV head): enough warps for the most chunks any sequence can have, and
-    // about two CTAs per SM over the batch (this choice changes no result)
-    const int64_t most = std::min<int64_t>(C, (max_len + kFdMinChunk - 1) / kFdMinChunk);
-    const int64_t fill = std::max<int64_t>(1, (2LL * sms) / (static_cast<int64_t>(B) * n_kv_heads));
-    const int64_t per_head = std::max<int64_t>(1, std::min<int64_t>(fill, (most + kFdWarps - 1) / kFdWarps));
 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -540,12 +661,29 @@ extern "C" q4_status q4_flash_decode(const uint16_t* Q, const uint16_t* K_cache,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
 
-    cfg.gridDim = dim3(static_cast<unsigned>(per_head), static_cast<unsigned>(n_kv_heads), static_cast<unsigned>(B));
+    cfg.gridDim = dim3(1u, static_cast<unsigned>(n_kv_heads), static_cast<unsigned>(B));
     cfg.blockDim = dim3(kFdWarps * 32);
-    cfg.dynamicSmemBytes = static_cast<size_t>(kFdWarps) * kFdStages * head_dim * 64;  // 96 KB at head_dim 128
+    const bool bulk = fd_bulk();
+    const int stages = bulk ? kFdStages : fd_stages();
+    const int slot = head_dim == 64 ? (bulk ? FdSlot<64, true>::kBytes : FdSlot<64, false>::kBytes)
+                                    : (bulk ? FdSlot<128, true>::kBytes : FdSlot<128, false>::kBytes);
+    cfg.dynamicSmemBytes = static_cast<size_t>(kFdWarps) * stages * (slot + (bulk ? 8 : 0));
     using SplitFn = void (*)(FdParams);
-    const SplitFn split = head_dim == 64 ? q4_flash_split_kernel<64, kFdStages> : q4_flash_split_kernel<128, kFdStages>;
+    const SplitFn split =
+        head_dim == 64 ? (bulk ? q4_flash_split_kernel<64, kFdStages, true>
+                               : stages == 2 ? q4_flash_split_kernel<64, 2, false> : q4_flash_split_kernel<64, 3, false>)
+                       : (bulk ? q4_flash_split_kernel<128, kFdStages, true>
+                               : stages == 2 ? q4_flash_split_kernel<128, 2, false>
+                                             : q4_flash_split_kernel<128, 3, false>);
     if (!smem_limit_raised(split, cfg.dynamicSmemBytes)) return Q4_ERR_CUDA;
+    // CTAs per (sequence, KV head): enough warps for the most chunks any sequence can have, and
+    // one full wave of resident CTAs over the batch (this choice changes no result)
+    const int resident = resident_ctas(split, cfg.dynamicSmemBytes);
+    if (resident <= 0) return Q4_ERR_CUDA;
+    const int64_t most = std::min<int64_t>(C, (max_len + kFdMinChunk - 1) / kFdMinChunk);
+    const int64_t fill = std::max<int64_t>(1, (static_cast<int64_t>(resident) * sms) / (static_cast<int64_t>(B) * n_kv_heads));
+    const int64_t per_head = std::max<int64_t>(1, std::min<int64_t>(fill, (most + kFdWarps - 1) / kFdWarps));
+    cfg.gridDim.x = static_cast<unsigned>(per_head);
     if (cudaLaunchKernelEx(&cfg, split, p) != cudaSuccess) return Q4_ERR_CUDA;
 
     cfg.gridDim = dim3(static_cast<unsigned>(n_q_heads), static_cast<unsigned>(B));

@@ -130,48 +130,7 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
     }
 }
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_barrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// Wait for the phase with the given parity to complete, at most `limit` polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
-    const uint32_t a = smem_addr(bar);
-    for (uint32_t it = 0; it < limit; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(done)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (done) return true;
-    }
-    return false;
-}
-
 __device__ __forceinline__ void report_timeout() { atomicOr(&g_q4_device_error, 1u); }
-
-// 1-D bulk copy global -> shared, completion counted on `bar` (bytes: multiple of 16).
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
 
 __device__ __forceinline__ uint4 lds128(const unsigned char* p) {
     uint4 r;
@@ -3167,7 +3126,10 @@ extern "C" q4_status q4_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return Q4_ERR_CUDA;
     unsigned v = 0;
     if (cudaMemcpyFromSymbol(&v, g_q4_device_error, sizeof v) != cudaSuccess) return Q4_ERR_CUDA;
-    if (v == 0) return Q4_OK;
+    const int attn = q4i_attn_take_error();
+    if (attn < 0) return Q4_ERR_CUDA;
+    if (v == 0 && attn == 0) return Q4_OK;
+    if (v == 0) return Q4_ERR_TIMEOUT;
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_q4_device_error, &zero, sizeof zero) != cudaSuccess) return Q4_ERR_CUDA;
     return Q4_ERR_TIMEOUT;

@@ -165,6 +165,22 @@ def test_graph_replay_with_new_lengths(q4):
         assert np.array_equal(got, run(q4, Q, K, V, nl)), new
 
 
+@pytest.mark.parametrize("fill", ["0", "1"])
+def test_both_ring_fills_give_the_same_bits(q4, fill, monkeypatch):
+    # bulk row copies (default) and per-lane cp.async fill the ring with the same data
+    Q, K, V, lens = synthetic.attention_problem(3, 24, 6, 128, 700, [700, 333, 17], 110)
+    ref = run(q4, Q, K, V, lens)
+    monkeypatch.setenv("Q4_FD_BULK", fill)
+    for stages in ("2", "3"):
+        monkeypatch.setenv("Q4_FD_STAGES", stages)
+        assert np.array_equal(run(q4, Q, K, V, lens), ref), (fill, stages)
+
+
+def test_device_status_clean_after_calls(q4):
+    check(q4, 2, 8, 2, 64, 300, [300, 2], 120)
+    q4.device_status()
+
+
 def test_long_cache_batch_8(q4):
     """Batch 8 over an 8,192-position cache (the bench's long case), ragged, all 192 heads."""
     lens = [8192, 8000, 4096, 1, 2000, 8191, 7777, 16]
