@@ -44,6 +44,7 @@ LAYERS = synthetic.LAYERS
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SRC = os.path.join(ROOT, "int4_weight_only_q4_gb300", "csrc", "q4_gemv.cu")
+KERNEL_HDR = os.path.join(os.path.dirname(KERNEL_SRC), "q4_common.cuh")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -165,7 +166,7 @@ def measured_peak_gbs():
 
 def kernel_src_sha() -> str:
     h = hashlib.sha256()
-    for f in (KERNEL_SRC,):
+    for f in (KERNEL_SRC, KERNEL_HDR):
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
