@@ -32,12 +32,13 @@
 // of the head dimension as the keys.  The partial o is stored in the accumulator's own order
 // (see fd_dim) and mapped back to head dimensions by the combine kernel.
 //
-// Combine kernel: one CTA of 512 threads per (query head, sequence):
-//     O = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c,   M = max_c m_c.
-// Each output element is summed by 512/D threads over interleaved chunks, their sums added in
-// thread order.  The partials' loads (up to 48 per thread) go out before, and together with, the
-// single parallel pass over all chunks' (m, l); the maximum and the denominator are fixed-order
-// block reductions.  Two dependent memory round trips in all for up to 192 chunks (D = 128).
+// Combine kernel: one CTA per (query head, sequence), 512 threads (256 when the pairs exceed one
+// wave of SMs):   O = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c,   M = max_c m_c.
+// The chunks fall into 512/D classes (chunk index modulo 512/D); each class is summed in chunk
+// order and the classes in class order, for the outputs and the denominator alike, so the bits do
+// not depend on the thread count.  The partials' loads (48 per thread per round) go out before,
+// and together with, the single parallel pass over all chunks' (m, l): two dependent memory round
+// trips in all for up to 192 chunks (D = 128, 512 threads).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -58,7 +59,6 @@ namespace {
 
 constexpr int kFdWarps = 4;
 constexpr int kFdStages = 3;           // ring slots per warp: two tiles in flight while one is used
-constexpr int kFdCombineThreads = 512;
 constexpr int kFdMaxGroup = 16;        // query heads per KV head: one 16-row tensor-core tile
 constexpr int kFdMaxChunks = 4096;
 constexpr int kFdMinChunk = 32;        // positions: at least two tiles per chunk
@@ -405,10 +405,10 @@ __global__ void __launch_bounds__(kFdWarps * 32) q4_flash_split_kernel(const __g
     }
 }
 
-// fixed-order block reductions over kFdCombineThreads threads (the same tree for every call)
-template <bool MAX>
+// fixed-order block reductions over NT threads (the same tree for every call)
+template <bool MAX, int NT>
 __device__ __forceinline__ float block_reduce(float v, float* red) {
-    constexpr int kWarps = kFdCombineThreads / 32;
+    constexpr int kWarps = NT / 32;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float w = __shfl_xor_sync(0xffffffffu, v, o);
@@ -423,15 +423,21 @@ __device__ __forceinline__ float block_reduce(float v, float* red) {
     return r;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kFdCombineThreads) q4_flash_combine_kernel(const __grid_constant__ FdParams p) {
-    constexpr int kSplit = kFdCombineThreads / D;  // threads per output element
-    constexpr int kAhead = 48;                     // chunk partials per thread loaded before any use
-    constexpr int kBatch = 8;                      // beyond those: loads issued eight ahead of their FMAs
-    constexpr int kPer = kFdMaxChunks / kFdCombineThreads;
-    __shared__ float w_s[kFdMaxChunks];            // chunk maxima, then weights 2^(m_c - M)
-    __shared__ float red[kFdCombineThreads / 32];
-    __shared__ float osum[kSplit][D];
+template <int D, int NT>
+__global__ void __launch_bounds__(NT, 512 / NT) q4_flash_combine_kernel(const __grid_constant__ FdParams p) {
+    // Chunk c belongs to class c % kRes; every class is summed in increasing chunk order into its
+    // own accumulator and the classes are added in class order -- the same sums, in the same
+    // order, for either thread count, so the result does not depend on NT.
+    constexpr int kRes = 512 / D;        // classes
+    constexpr int kSplit = NT / D;       // threads per output element
+    constexpr int kMine = kRes / kSplit; // classes per thread: j, j + kSplit, ...
+    constexpr int kAhead = 48 / kMine;   // partials per class per round, all loaded before any use
+    constexpr int kPer = kFdMaxChunks / NT;
+    __shared__ float w_s[kFdMaxChunks];  // chunk maxima, then weights 2^(m_c - M)
+    __shared__ float l_s[kFdMaxChunks];  // chunk sums l_c
+    __shared__ float red[NT / 32];
+    __shared__ float osum[kRes][D];
+    __shared__ float lsum[kRes];
     grid_dependency_wait();  // the chunk partials
     allow_dependents();
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
@@ -444,66 +450,71 @@ __global__ void __launch_bounds__(kFdCombineThreads) q4_flash_combine_kernel(con
         return;
     }
     const size_t slot0 = (static_cast<size_t>(b) * p.Hkv + kvh) * p.C * g + row;  // chunk c: + c*g
-    const int j = tid / D, e = tid - j * D;  // thread (j, e) adds chunks j, j + kSplit, ... of entry e
+    const int j = tid / D, e = tid - j * D;
 
-    // the partials do not depend on the maximum: their loads go out first, with the (m, l) loads
-    float v[kAhead];
+    // a round: entry e of chunks cls + (r0 + i) kRes of this thread's classes
+    float v[kMine][kAhead];
+    auto load_round = [&](int r0) {
 #pragma unroll
-    for (int i = 0; i < kAhead; ++i) {
-        const int c = j + i * kSplit;
-        v[i] = c < used ? ld_dep_f32(p.part + (slot0 + static_cast<size_t>(c) * g) * D + e) : 0.f;
-    }
-    float mmax = -INFINITY, lv[kPer];
+        for (int k = 0; k < kMine; ++k)
+#pragma unroll
+            for (int i = 0; i < kAhead; ++i) {
+                const int c = j + k * kSplit + (r0 + i) * kRes;
+                v[k][i] = c < used ? ld_dep_f32(p.part + (slot0 + static_cast<size_t>(c) * g) * D + e) : 0.f;
+            }
+    };
+    // the partials do not depend on the maximum: the first round goes out with the (m, l) loads
+    load_round(0);
+    float mmax = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-        const int c = tid + i * kFdCombineThreads;
-        lv[i] = 0.f;
+        const int c = tid + i * NT;
         if (c < used) {
             const uint2 ml = ld_dep_u2(p.ml + (slot0 + static_cast<size_t>(c) * g) * 2);
             w_s[c] = __uint_as_float(ml.x);
-            lv[i] = __uint_as_float(ml.y);
+            l_s[c] = __uint_as_float(ml.y);
             mmax = fmaxf(mmax, w_s[c]);
         }
     }
-    // M = max_c m_c, weights w_c = 2^(m_c - M), L = sum_c w_c l_c
-    const float M = block_reduce<true>(mmax, red);
-    float lpart = 0.f;
+    const float M = block_reduce<true, NT>(mmax, red);  // a maximum: exact in any order
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-        const int c = tid + i * kFdCombineThreads;
-        if (c < used) {
-            const float w = ex2(w_s[c] - M);
-            w_s[c] = w;
-            lpart = fmaf(w, lv[i], lpart);
-        }
+        const int c = tid + i * NT;
+        if (c < used) w_s[c] = ex2(w_s[c] - M);
     }
-    const float L = block_reduce<false>(lpart, red);  // also orders the w_s writes before the reads
+    __syncthreads();
 
-    float o = 0.f;
+    float o[kMine], l[kMine];
 #pragma unroll
-    for (int i = 0; i < kAhead; ++i) {
-        const int c = j + i * kSplit;
-        if (c < used) o = fmaf(w_s[c], v[i], o);
+    for (int k = 0; k < kMine; ++k) o[k] = l[k] = 0.f;
+    for (int r0 = 0;;) {
+#pragma unroll
+        for (int k = 0; k < kMine; ++k)
+#pragma unroll
+            for (int i = 0; i < kAhead; ++i) {
+                const int c = j + k * kSplit + (r0 + i) * kRes;
+                if (c < used) {
+                    o[k] = fmaf(w_s[c], v[k][i], o[k]);
+                    l[k] = fmaf(w_s[c], l_s[c], l[k]);
+                }
+            }
+        r0 += kAhead;
+        if (r0 * kRes >= used) break;
+        load_round(r0);
     }
-    for (int c0 = j + kAhead * kSplit; c0 < used; c0 += kSplit * kBatch) {
-        float u[kBatch];
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int c = c0 + i * kSplit;
-            u[i] = c < used ? ld_dep_f32(p.part + (slot0 + static_cast<size_t>(c) * g) * D + e) : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int c = c0 + i * kSplit;
-            if (c < used) o = fmaf(w_s[c], u[i], o);
-        }
+    for (int k = 0; k < kMine; ++k) {
+        osum[j + k * kSplit][e] = o[k];
+        if (e == 0) lsum[j + k * kSplit] = l[k];
     }
-    osum[j][e] = o;
     __syncthreads();
     if (tid < D) {
-        float r = osum[0][tid];
+        float r = osum[0][tid], L = lsum[0];
 #pragma unroll
-        for (int i = 1; i < kSplit; ++i) r += osum[i][tid];
+        for (int i = 1; i < kRes; ++i) {
+            r += osum[i][tid];
+            L += lsum[i];
+        }
         out[fd_dim(tid)] = r / L;
     }
 }
@@ -555,6 +566,14 @@ int resident_ctas(void (*fn)(FdParams), size_t smem) {
 bool fd_bulk() {
     const char* v = std::getenv("Q4_FD_BULK");
     return !(v && *v && std::atoi(v) == 0);
+}
+
+// threads per combine CTA for this many (query head, sequence) pairs (Q4_FD_COMBINE = 256 or
+// 512 overrides)
+int fd_combine_threads(int64_t pairs, int sms) {
+    const char* v = std::getenv("Q4_FD_COMBINE");
+    if (v && *v) return std::atoi(v) == 256 ? 256 : 512;
+    return pairs <= sms ? 512 : 256;
 }
 
 // ring slots per warp of the cp.async fill (Q4_FD_STAGES = 2 or 3)
@@ -686,10 +705,16 @@ extern "C" q4_status q4_flash_decode(const uint16_t* Q, const uint16_t* K_cache,
     cfg.gridDim.x = static_cast<unsigned>(per_head);
     if (cudaLaunchKernelEx(&cfg, split, p) != cudaSuccess) return Q4_ERR_CUDA;
 
+    // combine: 512-thread CTAs (one per SM) while the (query head, sequence) pairs fit in one
+    // wave, else 256-thread CTAs (two per SM); the order of every sum is fixed by D and the
+    // thread count, and so by B and the SM count only
+    const int nt = fd_combine_threads(static_cast<int64_t>(B) * n_q_heads, sms);
     cfg.gridDim = dim3(static_cast<unsigned>(n_q_heads), static_cast<unsigned>(B));
-    cfg.blockDim = dim3(kFdCombineThreads);
+    cfg.blockDim = dim3(static_cast<unsigned>(nt));
     cfg.dynamicSmemBytes = 0;
-    const cudaError_t e = head_dim == 64 ? cudaLaunchKernelEx(&cfg, q4_flash_combine_kernel<64>, p)
-                                         : cudaLaunchKernelEx(&cfg, q4_flash_combine_kernel<128>, p);
-    return e == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
+    using CombineFn = void (*)(FdParams);
+    const CombineFn comb = head_dim == 64 ? (nt == 512 ? q4_flash_combine_kernel<64, 512> : q4_flash_combine_kernel<64, 256>)
+                                          : (nt == 512 ? q4_flash_combine_kernel<128, 512>
+                                                       : q4_flash_combine_kernel<128, 256>);
+    return cudaLaunchKernelEx(&cfg, comb, p) == cudaSuccess ? Q4_OK : Q4_ERR_CUDA;
 }

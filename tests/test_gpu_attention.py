@@ -176,6 +176,19 @@ def test_both_ring_fills_give_the_same_bits(q4, fill, monkeypatch):
         assert np.array_equal(run(q4, Q, K, V, lens), ref), (fill, stages)
 
 
+def test_combine_thread_counts_give_the_same_bits(q4, monkeypatch):
+    # the combine sums chunk classes in a fixed order whatever its CTA size (512 or 256 threads)
+    Q, K, V, lens = synthetic.attention_problem(2, 24, 6, 128, 3000, [3000, 1111], 130)
+    Q64, K64, V64, lens64 = synthetic.attention_problem(2, 8, 2, 64, 3000, [2999, 400], 131)
+    for nc in (0, 16, 4096):
+        monkeypatch.setenv("Q4_FD_COMBINE", "512")
+        a = run(q4, Q, K, V, lens, n_chunks=nc)
+        a64 = run(q4, Q64, K64, V64, lens64, n_chunks=nc)
+        monkeypatch.setenv("Q4_FD_COMBINE", "256")
+        assert np.array_equal(run(q4, Q, K, V, lens, n_chunks=nc), a), nc
+        assert np.array_equal(run(q4, Q64, K64, V64, lens64, n_chunks=nc), a64), nc
+
+
 def test_device_status_clean_after_calls(q4):
     check(q4, 2, 8, 2, 64, 300, [300, 2], 120)
     q4.device_status()
