@@ -389,15 +389,17 @@ q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float* Y, int32_
  *            positions 0..len_b-1 are read.  len_b = 0 gives O[b] = 0.
  *   head_dim 64 or 128;  1 <= n_q_heads / n_kv_heads <= 16 (a whole multiple);
  *   B, n_kv_heads 1..65535;  1 <= max_len <= 2^30;  scale finite.
- *   n_chunks chunks per KV head, 1..4096, or 0 for the default of about two
- *            CTAs per SM for one sequence (q4_flash_decode_chunks reports it).
- *            The chunk length is ceil(len_b / chunks) rounded up to 16, so a
- *            sequence's result does not depend on B or on the other sequences.
+ *   n_chunks chunks per KV head at most, 1..4096, or 0 for the default of
+ *            about eight per SM for one sequence (q4_flash_decode_chunks
+ *            reports it).  The chunk length is ceil(len_b / chunks) rounded up
+ *            to 16 and at least 32 positions, so a sequence's result does not
+ *            depend on B or on the other sequences.
  *   O        device fp32 [B, n_q_heads, head_dim], 4-byte aligned.
  *   ws       device workspace, 16-byte aligned, of ws_bytes >=
  *            q4_flash_decode_workspace_bytes(...) (no initial content needed).
  * Two kernels on `stream` (chained by programmatic dependent launch); nothing
- * allocated.  Q4_ERR_INVALID_ARG for null pointers or out-of-range B, heads,
+ * allocated.  Every device-side wait is bounded; one that gives up is reported
+ * by q4_device_status (Q4_ERR_TIMEOUT).  Q4_ERR_INVALID_ARG for null pointers or out-of-range B, heads,
  * group, chunks, max_len or scale; Q4_ERR_UNSUPPORTED_SHAPE for another
  * head_dim; Q4_ERR_MISALIGNED; Q4_ERR_WORKSPACE if ws_bytes is too small.
  */
