@@ -36,9 +36,9 @@
 // wave of SMs):   O = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c,   M = max_c m_c.
 // The chunks fall into 512/D classes (chunk index modulo 512/D); each class is summed in chunk
 // order and the classes in class order, for the outputs and the denominator alike, so the bits do
-// not depend on the thread count.  The partials' loads (48 per thread per round) go out before,
-// and together with, the single parallel pass over all chunks' (m, l): two dependent memory round
-// trips in all for up to 192 chunks (D = 128, 512 threads).
+// not depend on the thread count.  The first round of partials (48 per thread) and all chunks'
+// (m, l) are loaded together with the sequence's length, bounded by the chunk capacity: one
+// memory round trip for up to 192 chunks (D = 128, 512 threads) before the arithmetic.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -442,38 +442,49 @@ __global__ void __launch_bounds__(NT, 512 / NT) q4_flash_combine_kernel(const __
     allow_dependents();
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int g = p.g, kvh = h / g, row = h - kvh * g;
-    int len, cs, used;
-    fd_chunking(p, b, len, cs, used);
-    float* out = p.O + (static_cast<size_t>(b) * p.Hkv * g + h) * D;
-    if (used == 0) {  // empty cache: O = 0
-        if (tid < D) out[tid] = 0.f;
-        return;
-    }
     const size_t slot0 = (static_cast<size_t>(b) * p.Hkv + kvh) * p.C * g + row;  // chunk c: + c*g
     const int j = tid / D, e = tid - j * D;
 
-    // a round: entry e of chunks cls + (r0 + i) kRes of this thread's classes
+    // a round: entry e of chunks cls + (r0 + i) kRes of this thread's classes, below `bound`
     float v[kMine][kAhead];
-    auto load_round = [&](int r0) {
+    auto load_round = [&](int r0, int bound) {
 #pragma unroll
         for (int k = 0; k < kMine; ++k)
 #pragma unroll
             for (int i = 0; i < kAhead; ++i) {
                 const int c = j + k * kSplit + (r0 + i) * kRes;
-                v[k][i] = c < used ? ld_dep_f32(p.part + (slot0 + static_cast<size_t>(c) * g) * D + e) : 0.f;
+                v[k][i] = c < bound ? ld_dep_f32(p.part + (slot0 + static_cast<size_t>(c) * g) * D + e) : 0.f;
             }
     };
-    // the partials do not depend on the maximum: the first round goes out with the (m, l) loads
-    load_round(0);
+    // The first round of partials and every chunk's (m, l) are loaded together with the length
+    // (one memory round trip, not two), bounded by the chunk capacity C: entries of chunks at or
+    // past the used count hold stale workspace data and are never read back below.
+    int len, cs, used;
+    fd_chunking(p, b, len, cs, used);
+    load_round(0, p.C);
+    float mraw[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int c = tid + i * NT;
+        mraw[i] = -INFINITY;
+        if (c < p.C) {
+            const uint2 ml = ld_dep_u2(p.ml + (slot0 + static_cast<size_t>(c) * g) * 2);
+            mraw[i] = __uint_as_float(ml.x);
+            l_s[c] = __uint_as_float(ml.y);
+        }
+    }
+    float* out = p.O + (static_cast<size_t>(b) * p.Hkv * g + h) * D;
+    if (used == 0) {  // empty cache: O = 0
+        if (tid < D) out[tid] = 0.f;
+        return;
+    }
     float mmax = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const int c = tid + i * NT;
         if (c < used) {
-            const uint2 ml = ld_dep_u2(p.ml + (slot0 + static_cast<size_t>(c) * g) * 2);
-            w_s[c] = __uint_as_float(ml.x);
-            l_s[c] = __uint_as_float(ml.y);
-            mmax = fmaxf(mmax, w_s[c]);
+            w_s[c] = mraw[i];
+            mmax = fmaxf(mmax, mraw[i]);
         }
     }
     const float M = block_reduce<true, NT>(mmax, red);  // a maximum: exact in any order
@@ -500,7 +511,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) q4_flash_combine_kernel(const __
             }
         r0 += kAhead;
         if (r0 * kRes >= used) break;
-        load_round(r0);
+        load_round(r0, used);
     }
 #pragma unroll
     for (int k = 0; k < kMine; ++k) {
