@@ -37,6 +37,12 @@ def _stream_ptr(stream) -> int:
 
 
 def _ptr(t: torch.Tensor) -> int:
+    """Device address of a tensor handed to the library, which reads and writes it from kernels on
+    the current device: anything else is refused here (a host address would fault the GPU)."""
+    if not t.is_cuda:
+        raise TypeError(f"expected a CUDA tensor, got one on {t.device}")
+    if t.device.index != torch.cuda.current_device():
+        raise TypeError(f"tensor on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
     return int(t.data_ptr())
 
 

@@ -155,3 +155,25 @@ def test_host_validation_before_any_cuda_call():
     assert L.q4_gemv(ctypes.byref(m), 16, 16, None, 0, None) == _lib.Q4_ERR_MISALIGNED
     info = _lib.q4_plan_info()
     assert L.q4_plan(10, 200, ctypes.byref(info)) == _lib.Q4_ERR_UNSUPPORTED_SHAPE
+
+
+def test_binding_refuses_host_tensors_before_any_library_call():
+    """Every wrapper hands device addresses to kernels; a host tensor would fault the GPU, so the
+    binding refuses it (no GPU needed: the check runs before the library is called)."""
+    import torch
+    import int4_weight_only_q4_gb300 as q4
+    w, x = synthetic.random_shape_problem(32, 256, 2, seed=3)
+    W = q4.QuantizedMatrix.from_packed(*q4.pack_host(w), device="cpu", tiled=False)
+    X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    Y = torch.empty((2, 32), dtype=torch.float32)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        q4.gemm_skinny(W, X, Y, workspace=q4.Workspace(0, "cpu"))
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        q4.argmax(Y)
+    Qb = torch.zeros((1, 8, 64), dtype=torch.bfloat16)
+    Kb = torch.zeros((1, 2, 16, 64), dtype=torch.bfloat16)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        q4.flash_decode(Qb, Kb, Kb, torch.zeros(1, dtype=torch.int32), n_chunks=4,
+                        workspace=q4.Workspace(1 << 16, "cpu"))
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        q4.sample_topk(Y, 4, 1.0, torch.zeros((2, 4)))
