@@ -5,8 +5,8 @@ Step (what one timed iteration is): one synthetic decode step -- 36 layers x
 {fused qkv+gate+up 25,088x3072, o-proj 3072x3072, down 3072x8192} -- plus the
 wide output head (65,536x3072) and the argmax over its logits, all int4
 group-128 with fp16 scale/min, batch 1, replayed as one CUDA graph (the
-rumik-oss-1 page, "Step 3": 108 projections and the audio head in one CUDA
-graph).  Every step streams 2.243 GB of weights, far above the 129 MB L2, so
+rumik-oss-1 page, "Step 3": the whole step -- every projection plus the head --
+captured as a single CUDA graph).  Every step streams 2.243 GB of weights, far above the 129 MB L2, so
 no L2 flush is needed between steps.
 
 Metric: achieved HBM GB/s of algorithmic bytes (weights + activations +

@@ -96,8 +96,8 @@ typedef struct {
 } q4_plan_info;
 
 /*
- * q4_pack_host -- the offline export job ("Step 3": a short CPU job exported
- * the weights to a plain int4 format).  Host memory only.
+ * q4_pack_host -- the offline export job ("Step 3": the int4 file is written
+ * once, on the CPU, before the GPU sees the weights).  Host memory only.
  *   w       host fp32 [N, K] row-major, finite.
  *   codes   host out uint8 [N, K/2]; scales, mins host out uint16 [N, K/128].
  *   n_threads  worker threads (<= 0: all hardware threads).
@@ -284,9 +284,9 @@ q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* st
 
 /*
  * q4_gemm_prefill -- Y[m, :] = W X[m, :] for a prompt of M tokens (the rumik-oss-1
- * write-up, "Step 8: a prefill that stays int4": the weights stay int4, are
- * unpacked a group at a time onto the tensor cores, and scale and minimum are
- * applied to the result).  fp32 accumulation; a tensor-core GEMM (mma.sync),
+ * write-up, "Step 8: a prefill that stays int4": no dequantised copy of the
+ * weights; each group is expanded in registers for the tensor cores and its
+ * scale and minimum are folded into the fp32 result).  fp32 accumulation; a tensor-core GEMM (mma.sync),
  * not bound by the weight bytes once M is large.
  *   W   host pointer; W->tiled (device) is required.
  *   X   device bf16 bits [M, K], 16-byte aligned;  Y device fp32 [M, N].
@@ -300,9 +300,9 @@ q4_status q4_gemm_prefill(const q4_matrix* W, const uint16_t* X, int64_t M, floa
 
 /*
  * q4_sample_topk -- top-k sampling with the Gumbel-max trick over logits
- * (rumik-oss-1 write-up, "Step 4": top-k sampling on the GPU with the
- * Gumbel-max trick; "Steps 9-10": the top k found by sorting 64-bit keys that
- * pack the float bits with the index).  Per batch row b of Y [B, N] (device
+ * (rumik-oss-1 write-up, "Step 4": the next token drawn on the device, top-k
+ * plus Gumbel-max; "Steps 9-10": candidates ranked by 64-bit integer keys
+ * built from each logit's bit pattern and its position).  Per batch row b of Y [B, N] (device
  * fp32): rank the logits -- NaN above every number, larger first, the lower
  * index first among equal values (the q4_argmax_f32 order) -- and keep the first
  * k; score rank r as fp32(fp32(Y[b, i_r] * inv_temperature) + noise[b, r]), two
@@ -321,9 +321,9 @@ q4_status q4_sample_topk(const float* Y, int B, int64_t N, int k, float inv_temp
 /* ------------------------------------------------------------------------
  * The int8 output head.  The rumik-oss-1 write-up keeps every projection in
  * int4 except the output head ("Steps 9-10: streaming to the speaker": the
- * audio head moved to int8 with its own CUDA kernel because int4 was
- * measurably too lossy there; "Step 2": int8 weights as torchao quantized
- * tensors).  Format (torchao's int8 weight-only scheme; the pages give no more
+ * audio head got int8 weights and a dedicated CUDA kernel, int4 having cost that
+ * matrix clearly more accuracy than the others; "Step 2": int8 weights as
+ * torchao quantized tensors).  Format (torchao's int8 weight-only scheme; the pages give no more
  * detail): per output row n an fp16 scale s_n = fp16(max_k |w[n,k]| / 127),
  * codes c = clamp(rint(w / s_n), -127, 127) as int8, w_hat = c * s_n.
  * ------------------------------------------------------------------------ */
@@ -374,9 +374,9 @@ q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float* Y, int32_
 /*
  * q4_flash_decode -- one decode step of grouped-query attention over a KV
  * cache, split over chunks of the cache (the rumik-oss-1 write-up, "Step 6:
- * flash-decoding for long clips": the cache of each KV head split into
- * chunks, the query heads that share a KV head computed in one tensor-core
- * tile, the chunks' partial results merged by a second kernel).  For every
+ * flash-decoding for long clips": each KV head's cache cut into pieces worked
+ * on in parallel, the grouped query heads forming the rows of one
+ * matrix-multiply tile, a separate small kernel merging the pieces).  For every
  * sequence b and query head h, with g = n_q_heads / n_kv_heads:
  *     O[b,h,:] = sum_{p < len_b} softmax_p(scale * <Q[b,h,:], K[b,h/g,p,:]>) V[b,h/g,p,:]
  * (query head h reads KV head h / g).  fp32 softmax and accumulation; the

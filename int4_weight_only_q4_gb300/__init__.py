@@ -5,9 +5,9 @@ only; every step of the computation runs in the library's CUDA kernels, and
 the host packer runs in the library's C++ code.  There is no CPU fallback:
 without the built library this package does not import.
 
-Weight format (rumik-oss-1 int4 engine page, "Step 3"): groups of 128 columns,
-an fp16 scale and an fp16 minimum per group, two 4-bit codes per byte (column
-2j in the low nibble), w = code * scale + min.
+Weight format (rumik-oss-1 int4 engine page, "Step 3"): for every row, each run of
+128 columns carries one fp16 scale and one fp16 minimum; codes are 4 bits, packed
+in pairs (column 2j in the low nibble), w = code * scale + min.
 """
 from __future__ import annotations
 

@@ -3,9 +3,9 @@
 // What is computed (rumik-oss-1 int4 engine page, rtts.neoandmatrix.me, "Step 6: flash-decoding
 // for long clips"):
 //     O[b, h, :] = sum_{p < len[b]} softmax_p(scale * <Q[b,h,:], K[b,h/g,p,:]>) V[b,h/g,p,:]
-// with g = Hq / Hkv query heads per KV head.  The page splits the cache of every KV head into
-// chunks, computes the query heads that share a KV head together in one tensor-core tile, and
-// merges the chunks' partial results in a small second kernel; so does this file.
+// with g = Hq / Hkv query heads per KV head.  As on the page, each KV head's cache is cut into
+// pieces (chunks) processed in parallel, the g grouped query heads are the rows of one
+// matrix-multiply tile, and a separate small kernel merges the per-chunk results.
 //
 // Chunking: chunk length cs = max(ceil(len / C) rounded up to 16, a minimum length), C chunks
 // per KV head at most.  It depends on len[b], C and the minimum and nothing else (never on B).

@@ -1908,8 +1908,9 @@ __global__ void __launch_bounds__(kSampleThreads) q4_sample_kernel(const float* 
 
 // ================================================================== int4 prefill GEMM
 // q4_prefill_kernel: Y[m, n] = sum_k w_hat[n, k] X[m, k] for a prompt of M tokens (the rumik-oss-1
-// write-up, "Step 8: a prefill that stays int4": the weights stay int4, a group is unpacked at a
-// time onto the tensor cores, and scale and minimum are applied to the result).  The tokens are
+// write-up, "Step 8: a prefill that stays int4": no dequantised copy of the weights; each group is
+// expanded in registers for the tensor cores and its scale and minimum are folded into the fp32
+// result).  The tokens are
 // taken 8 at a time (a "token block"), each block prepared by q4_xprep_kernel exactly like a B = 8
 // decode activation (layout LM: scaled per token, group sums divided by the token factor).  A CTA of
 // WARPS warps covers WARPS 16-row tiles (one per warp) and TBS token blocks; for every 128-column

@@ -1,8 +1,8 @@
 // Host side of libq4.so: the offline int4 export (q4_pack_host) and status strings.
 //
 // The export follows the rumik-oss-1 int4 engine page (rtts.neoandmatrix.me,
-// "Step 3: an int4 file and a first kernel"): groups of 128 columns, an fp16
-// scale and an fp16 minimum per group, two 4-bit codes per byte.  The
+// "Step 3: an int4 file and a first kernel"): for every row, each run of 128
+// columns carries one fp16 scale and one fp16 minimum; 4-bit codes packed in pairs.  The
 // arithmetic is plain IEEE double; this file is compiled with
 // -ffp-contract=off so no multiply-add is fused and the result is the same on
 // x86-64 and aarch64 hosts.

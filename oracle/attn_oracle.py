@@ -4,10 +4,10 @@ TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's CPU
 baseline may import this module.  The library never imports it, and it imports
 nothing from the library.
 
-The rumik-oss-1 write-up, "Step 6: flash-decoding for long clips", splits the
-attention of one decode step over chunks of the cache per KV head, computes the
-query heads that share a KV head together on the tensor cores, and merges the
-chunks' partial results in a second kernel.  Splitting a softmax-weighted sum
+The rumik-oss-1 write-up, "Step 6: flash-decoding for long clips", cuts each KV
+head's cache into pieces that are processed in parallel, lets the grouped query
+heads of one KV head form the rows of a single matrix-multiply tile, and merges
+the per-piece results with a separate small kernel.  Splitting a softmax-weighted sum
 into chunks and merging them reaches the same value as the one-pass sum (up to
 rounding), so this oracle is the definition of the attention output itself:
 

@@ -9,9 +9,10 @@ Everything is computed in float64 with numpy, one obvious step at a time, in
 the order the method is described on the rumik-oss-1 int4 engine page
 (rtts.neoandmatrix.me):
 
-  * "Step 3: an int4 file and a first kernel": every projection is quantised
-    in groups of 128 columns with an fp16 scale and an fp16 minimum per group,
-    two 4-bit codes per byte.  Dequantisation is w = code * scale + min.
+  * "Step 3: an int4 file and a first kernel": every projection's rows are cut
+    into runs of 128 columns, each run carrying one fp16 scale and one fp16
+    minimum; the 4-bit codes are packed in pairs.  Dequantisation is
+    w = code * scale + min.
   * "Step 7: why the GEMV was stuck": the GEMV is y = W x; known-answer inputs
     (e.g. all-zero codes leave only the minimum term) catch a min term that
     is counted the wrong number of times.

@@ -6,9 +6,9 @@ never imports it, and it imports nothing from the library.
 
 The rumik-oss-1 int4 engine write-up (rtts.neoandmatrix.me) keeps every
 projection in int4 except the output head: "Steps 9-10: streaming to the
-speaker" moves the audio head to int8 with its own CUDA kernel because int4 was
-measurably too lossy there, and the closing advice repeats that the output head
-needed int8.  "Step 2: int8 and int4 weights" obtains its int8 weights from
+speaker" moves the audio head to int8 with its own CUDA kernel, int4 having
+cost that matrix clearly more accuracy than the others, and the closing advice
+names the output head as the one matrix that needed int8.  "Step 2: int8 and int4 weights" obtains its int8 weights from
 torchao's quantized tensors.  The pages give no further detail of the int8
 format; the reading taken here (listed in the design notes) is torchao's int8
 weight-only scheme:

@@ -6,8 +6,9 @@ nothing from the library.
 
 The rumik-oss-1 write-up samples the next token on the GPU: "Step 4: our own
 engine speaks" lists top-k sampling with the Gumbel-max trick, and "Steps 9-10:
-streaming to the speaker" replaces the sampler by kernels that find the top k by
-sorting 64-bit keys packing the float bits with the index.  Readings where the
+streaming to the speaker" moves the sampler into kernels that rank candidates
+by 64-bit integer keys built from each logit's bit pattern and its position.
+Readings where the
 pages are silent (listed in the design notes):
 
   * ranking: NaN above every number, then larger values, then the lower index

@@ -1,7 +1,8 @@
 """GPU parity of the int4 prefill GEMM (q4_gemm_prefill) against the fp64 CPU oracle.
 
-The rumik-oss-1 write-up's "Step 8: a prefill that stays int4": the prompt's M tokens times the
-int4 weights on the tensor cores, scale and minimum applied to the result.  The oracle is the
+The rumik-oss-1 write-up's "Step 8: a prefill that stays int4": the prompt's M tokens multiply
+the int4 weights directly (no dequantised copy), on the tensor cores, with each group's scale and
+minimum folded into the fp32 result.  The oracle is the
 same dequantise-then-matmul (gemv_packed takes any number of activation rows).  Tolerance as for
 the GEMV: max relative error <= 2e-3 per output (floor 1% of the output RMS).
 """
