@@ -164,10 +164,36 @@ def measured_peak_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments and blank runs (string and character literals kept),
+    so that the hash below changes with the code and not with its comments."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            i = src.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_src_sha() -> str:
+    """Hash of the GEMV kernels' code (comments excluded): profiled counters stay valid until it
+    changes."""
     h = hashlib.sha256()
     for f in (KERNEL_SRC, KERNEL_HDR):
-        h.update(open(f, "rb").read())
+        h.update(strip_comments(open(f, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 
