@@ -403,7 +403,11 @@ q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float* Y, int32_
  * group, chunks, max_len or scale; Q4_ERR_UNSUPPORTED_SHAPE for another
  * head_dim; Q4_ERR_MISALIGNED; Q4_ERR_WORKSPACE if ws_bytes is too small.
  */
+/* Chunks per KV head that q4_flash_decode uses for this request (n_chunks itself
+ * when > 0; the default needs the current device's SM count); 0 for invalid
+ * arguments or when the device cannot be queried. */
 int q4_flash_decode_chunks(int n_kv_heads, int n_chunks);
+/* Workspace bytes for these sizes (0 for invalid arguments, as above). */
 size_t q4_flash_decode_workspace_bytes(int B, int n_q_heads, int n_kv_heads, int head_dim, int n_chunks);
 q4_status q4_flash_decode(const uint16_t* Q, const uint16_t* K_cache, const uint16_t* V_cache,
                           const int32_t* lengths, int B, int n_q_heads, int n_kv_heads, int head_dim,
