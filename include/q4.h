@@ -399,7 +399,9 @@ q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float* Y, int32_
  *            q4_flash_decode_workspace_bytes(...) (no initial content needed).
  * Two kernels on `stream` (chained by programmatic dependent launch); nothing
  * allocated.  Every device-side wait is bounded; one that gives up is reported
- * by q4_device_status (Q4_ERR_TIMEOUT).  Q4_ERR_INVALID_ARG for null pointers or out-of-range B, heads,
+ * by q4_device_status (Q4_ERR_TIMEOUT).  The first call per device and head
+ * size raises the split kernel's shared-memory limit and queries its
+ * occupancy: make it before any stream capture.  Q4_ERR_INVALID_ARG for null pointers or out-of-range B, heads,
  * group, chunks, max_len or scale; Q4_ERR_UNSUPPORTED_SHAPE for another
  * head_dim; Q4_ERR_MISALIGNED; Q4_ERR_WORKSPACE if ws_bytes is too small.
  */
