@@ -3,9 +3,9 @@
  * GEMM (batch 1..8) for small-batch autoregressive decoding on GB300 (sm_103a).
  *
  * Weight format (rumik-oss-1 int4 engine page, rtts.neoandmatrix.me,
- * "Step 3: an int4 file and a first kernel"): every projection is quantised in
- * groups of 128 consecutive columns of a row, with an fp16 scale and an fp16
- * minimum per group and two 4-bit codes per byte; a weight is
+ * "Step 3: an int4 file and a first kernel"): each row of a projection is cut
+ * into runs of 128 columns; a run has one fp16 scale and one fp16 minimum, and
+ * its 4-bit codes are packed in pairs; a weight is
  *     w = code * scale + min.
  *
  * Canonical layout used by every call ("L0"):
@@ -32,6 +32,9 @@
  *     on the batched matvec that first accumulated in a different order).
  *   - Calls are stateless apart from the caller's workspace and may be
  *     issued from several host threads on different streams.
+ *   - Kernels that need more than 48 KB of shared memory get that limit raised
+ *     (a function attribute, not stream work) on their first launch per
+ *     device: make each entry point's first call outside stream capture.
  */
 #ifndef Q4_H
 #define Q4_H
