@@ -267,6 +267,8 @@ q4_status q4_step_stream(const q4_matrix* mats, int n_mats, float* const* Y, int
  * different host threads -- race on it; serialise them.
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
+ * Only a successful lookup is kept (a failed one is tried again on the next
+ * call); a device reset invalidates it, so do not reset a device this runs on.
  * Other errors as for q4_gemm_skinny; Q4_ERR_CUDA if the lookup fails.
  */
 q4_status q4_gemm_skinny_noalloc(const q4_matrix* W, const uint16_t* X, int B, float* Y,

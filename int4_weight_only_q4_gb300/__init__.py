@@ -171,14 +171,31 @@ def _as_bf16(x: torch.Tensor) -> torch.Tensor:
     return x
 
 
+def _check_x(X: torch.Tensor, K: int) -> int:
+    """Batch size of activations X ([K] or [B, K], bf16, contiguous) for a matrix of K columns."""
+    _as_bf16(X)
+    if X.dim() not in (1, 2) or X.shape[-1] != K:
+        raise ValueError(f"activations of shape {tuple(X.shape)} do not match a matrix of K = {K} columns")
+    return 1 if X.dim() == 1 else X.shape[0]
+
+
+def _check_y(Y: torch.Tensor, B: int, N: int) -> None:
+    """The kernels write B * N fp32 values from Y's first element on: refuse anything smaller, of
+    another dtype or not contiguous (a short buffer would be written past its end)."""
+    if Y.dtype != torch.float32 or not Y.is_contiguous():
+        raise TypeError("outputs must be a contiguous torch.float32 CUDA tensor")
+    if Y.numel() < B * N:
+        raise ValueError(f"output of {Y.numel()} elements is smaller than B * N = {B} * {N}")
+
+
 # ---------------------------------------------------------------------------- calls
 def gemm_skinny(W: QuantizedMatrix, X: torch.Tensor, Y: torch.Tensor | None = None,
                 workspace: Workspace | None = None, stream=None) -> torch.Tensor:
     """Y[b] = W X[b] for X bf16 [B, K] (1 <= B <= 8); Y fp32 [B, N]."""
-    X = _as_bf16(X)
-    B = 1 if X.dim() == 1 else X.shape[0]
+    B = _check_x(X, W.K)
     if Y is None:
         Y = torch.empty((B, W.N), dtype=torch.float32, device=X.device)
+    _check_y(Y, B, W.N)
     if workspace is None and workspace_bytes(W.N, W.K, B):
         workspace = Workspace(workspace_bytes(W.N, W.K, B), X.device)
     ws_p, ws_n = _ws_args(workspace)
@@ -191,8 +208,8 @@ def gemm_skinny(W: QuantizedMatrix, X: torch.Tensor, Y: torch.Tensor | None = No
 def gemm_skinny_noalloc(W: QuantizedMatrix, X: torch.Tensor, Y: torch.Tensor, stream=None) -> torch.Tensor:
     """Y = W X with no workspace: the library's fixed scratch array instead (see q4.h for its
     limits and for the rule that calls overlapping on the GPU race)."""
-    X = _as_bf16(X)
-    B = 1 if X.dim() == 1 else X.shape[0]
+    B = _check_x(X, W.K)
+    _check_y(Y, B, W.N)
     m = W.c_struct()
     check(lib.q4_gemm_skinny_noalloc(ctypes.byref(m), _ptr(X), B, _ptr(Y), _stream_ptr(stream)),
           "q4_gemm_skinny_noalloc")
@@ -202,9 +219,11 @@ def gemm_skinny_noalloc(W: QuantizedMatrix, X: torch.Tensor, Y: torch.Tensor, st
 def gemv(W: QuantizedMatrix, x: torch.Tensor, y: torch.Tensor | None = None,
          workspace: Workspace | None = None, stream=None) -> torch.Tensor:
     """y = W x for x bf16 [K]; y fp32 [N]."""
-    x = _as_bf16(x)
+    if _check_x(x, W.K) != 1:
+        raise ValueError("gemv takes one activation vector")
     if y is None:
         y = torch.empty((W.N,), dtype=torch.float32, device=x.device)
+    _check_y(y, 1, W.N)
     if workspace is None and workspace_bytes(W.N, W.K, 1):
         workspace = Workspace(workspace_bytes(W.N, W.K, 1), x.device)
     ws_p, ws_n = _ws_args(workspace)
@@ -213,19 +232,37 @@ def gemv(W: QuantizedMatrix, x: torch.Tensor, y: torch.Tensor | None = None,
     return y
 
 
+def _check_i32(t: torch.Tensor, n: int, name: str) -> None:
+    if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() < n:
+        raise ValueError(f"{name} must be a contiguous int32 tensor of at least {n} elements")
+
+
+def _check_list(mats, Xs, Ys=None) -> int:
+    """One batch size for every matrix of a list, activations and outputs sized for each."""
+    if len(Xs) != len(mats) or (Ys is not None and len(Ys) != len(mats)):
+        raise ValueError("one activation tensor (and one output tensor) per matrix")
+    Bs = {_check_x(x, m.K) for x, m in zip(Xs, mats)}
+    if len(Bs) != 1:
+        raise ValueError(f"every activation tensor must have the same batch size, got {sorted(Bs)}")
+    B = Bs.pop()
+    for y, m in zip(Ys or [], mats):
+        _check_y(y, B, m.N)
+    return B
+
+
 def decode_step(mats, Xs, Ys, workspace: Workspace | None = None, stream=None, independent: bool = True) -> None:
     """Enqueue one decode step: Ys[i] = mats[i] Xs[i] for every matrix, in list order.
 
     independent=True: one persistent launch for the whole list (no Xs[j] may overlap any Ys[i]);
     False: one launch per matrix, so Ys[i] may feed Xs[j] for j > i."""
     n = len(mats)
-    B = Xs[0].shape[0] if Xs[0].dim() == 2 else 1
+    B = _check_list(mats, Xs, Ys)
     if workspace is None:
         need = decode_step_workspace_bytes([(m.N, m.K) for m in mats], B, independent)
         if need:
             workspace = Workspace(need, Xs[0].device)
     arr = (q4_matrix * n)(*[m.c_struct() for m in mats])
-    xp = (c_vp * n)(*[_ptr(_as_bf16(x)) for x in Xs])
+    xp = (c_vp * n)(*[_ptr(x) for x in Xs])
     yp = (c_vp * n)(*[_ptr(y) for y in Ys])
     ws_p, ws_n = _ws_args(workspace)
     flags = Q4_STEP_INDEPENDENT if independent else 0
@@ -241,9 +278,9 @@ def step_workspace_bytes(Ks, B: int) -> int:
 def step_prepare(mats, Xs, workspace: Workspace, stream=None) -> None:
     """Phase 1 of an independent decode step: stage every activation once into the workspace."""
     n = len(mats)
-    B = Xs[0].shape[0] if Xs[0].dim() == 2 else 1
+    B = _check_list(mats, Xs)
     arr = (q4_matrix * n)(*[m.c_struct() for m in mats])
-    xp = (c_vp * n)(*[_ptr(_as_bf16(x)) for x in Xs])
+    xp = (c_vp * n)(*[_ptr(x) for x in Xs])
     check(lib.q4_step_prepare(arr, n, xp, B, workspace.ptr(), workspace.nbytes, _stream_ptr(stream)),
           "q4_step_prepare")
 
@@ -251,6 +288,10 @@ def step_prepare(mats, Xs, workspace: Workspace, stream=None) -> None:
 def step_stream(mats, Ys, B: int, workspace: Workspace, stream=None) -> None:
     """Phase 2: Ys[i] = mats[i] x_i from the activations the last step_prepare staged."""
     n = len(mats)
+    if len(Ys) != n:
+        raise ValueError("one output tensor per matrix")
+    for y, m in zip(Ys, mats):
+        _check_y(y, B, m.N)
     arr = (q4_matrix * n)(*[m.c_struct() for m in mats])
     yp = (c_vp * n)(*[_ptr(y) for y in Ys])
     check(lib.q4_step_stream(arr, n, yp, B, workspace.ptr(), workspace.nbytes, _stream_ptr(stream)),
@@ -265,6 +306,7 @@ def argmax(Y: torch.Tensor, idx: torch.Tensor | None = None, stream=None) -> tor
     B, N = Y2.shape
     if idx is None:
         idx = torch.empty((B,), dtype=torch.int32, device=Y.device)
+    _check_i32(idx, B, "idx")
     check(lib.q4_argmax_f32(_ptr(Y2), B, N, _ptr(idx), _stream_ptr(stream)), "q4_argmax_f32")
     return idx
 
@@ -311,12 +353,15 @@ class Int8Head:
     def __call__(self, X: torch.Tensor, Y: torch.Tensor | None = None, idx: torch.Tensor | None = None,
                  logits: bool = True, argmax: bool = True, workspace: Workspace | None = None, stream=None):
         """Returns (Y or None, idx or None) for X bf16 [B, K]."""
-        X = _as_bf16(X)
-        B = 1 if X.dim() == 1 else X.shape[0]
+        B = _check_x(X, self.K)
         if logits and Y is None:
             Y = torch.empty((B, self.N), dtype=torch.float32, device=X.device)
         if argmax and idx is None:
             idx = torch.empty((B,), dtype=torch.int32, device=X.device)
+        if logits:
+            _check_y(Y, B, self.N)
+        if argmax:
+            _check_i32(idx, B, "idx")
         if workspace is None:
             workspace = self.workspace(B, X.device)
         ws_p, ws_n = _ws_args(workspace)
@@ -329,11 +374,11 @@ class Int8Head:
 def gemm_prefill(W: QuantizedMatrix, X: torch.Tensor, Y: torch.Tensor | None = None,
                  workspace: Workspace | None = None, stream=None) -> torch.Tensor:
     """Y [M, N] = X [M, K] W^T for a prompt of M tokens (q4_gemm_prefill, tensor-core GEMM)."""
-    X = _as_bf16(X)
+    M = _check_x(X, W.K)
     X2 = X if X.dim() == 2 else X.view(1, -1)
-    M = X2.shape[0]
     if Y is None:
         Y = torch.empty((M, W.N), dtype=torch.float32, device=X.device)
+    _check_y(Y, M, W.N)
     if workspace is None:
         workspace = Workspace(int(lib.q4_prefill_workspace_bytes(W.K, M)), X.device)
     ws_p, ws_n = _ws_args(workspace)
@@ -356,6 +401,11 @@ def sample_topk(Y: torch.Tensor, k: int, inv_temperature: float, noise: torch.Te
         token = torch.empty((B,), dtype=torch.int32, device=Y.device)
     if return_topk and topk is None:
         topk = torch.empty((B, k), dtype=torch.int32, device=Y.device)
+    if noise.numel() < B * k:
+        raise ValueError(f"noise must hold B * k = {B} * {k} values")
+    _check_i32(token, B, "token")
+    if topk is not None:
+        _check_i32(topk, B * k, "topk")
     check(lib.q4_sample_topk(_ptr(Y2), B, N, int(k), float(inv_temperature), _ptr(noise), _ptr(token),
                              _ptr(topk) if topk is not None else None, _stream_ptr(stream)), "q4_sample_topk")
     return (token, topk) if return_topk else token

@@ -2853,18 +2853,23 @@ extern "C" q4_status q4_step_stream(const q4_matrix* mats, int n_mats, float* co
 static constexpr size_t kNoallocScratchBytes = 512 * 1024;
 static __device__ __align__(256) unsigned char g_q4_noalloc_scratch[kNoallocScratchBytes];
 
-// Device address of the scratch on the current device, looked up once per device (with that
-// device current) on its first use; nullptr if the lookup failed.
+// Device address of the scratch on the current device, looked up (with that device current) on
+// the first call that finds none cached; nullptr if the lookup failed.  Only a successful lookup is
+// kept, so a failed one (say, one made during stream capture) is tried again by the next call.  A
+// device reset invalidates the cached address: the process must not reset a device it uses this on.
 static void* noalloc_scratch(int dev) {
     static void* addr[kMaxDevices];
-    static cudaError_t err[kMaxDevices];
-    static std::once_flag flags[kMaxDevices];
+    static std::mutex mu;
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::call_once(flags[dev], [dev] {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
         void* p = nullptr;
-        err[dev] = cudaGetSymbolAddress(&p, g_q4_noalloc_scratch);
-        addr[dev] = err[dev] == cudaSuccess ? p : nullptr;
-    });
+        if (cudaGetSymbolAddress(&p, g_q4_noalloc_scratch) == cudaSuccess) {
+            addr[dev] = p;
+        } else {
+            (void)cudaGetLastError();  // not sticky: clear it so that later checks do not see it
+        }
+    }
     return addr[dev];
 }
 
@@ -2879,6 +2884,7 @@ extern "C" q4_status q4_gemm_skinny_noalloc(const q4_matrix* W, const uint16_t* 
     if ((s = check_io(X, B, Y)) != Q4_OK) return s;
     const Knobs k = knobs();
     if (prep_bytes(W->K, batch_tile(k, 5, B)) > kNoallocScratchBytes) return Q4_ERR_WORKSPACE;
+    if (fault_injected()) return Q4_ERR_CUDA;
     int dev = 0;
     const int sms = device_sm_count(&dev);
     if (sms <= 0) return Q4_ERR_CUDA;

@@ -177,3 +177,46 @@ def test_binding_refuses_host_tensors_before_any_library_call():
                         workspace=q4.Workspace(1 << 16, "cpu"))
     with pytest.raises(TypeError, match="CUDA tensor"):
         q4.sample_topk(Y, 4, 1.0, torch.zeros((2, 4)))
+
+
+def test_binding_refuses_mis_sized_outputs_and_activations():
+    """A short or mistyped output buffer would be written past its end by the kernels: the binding
+    refuses it, and activations whose width is not the matrix's K, before any library call."""
+    import torch
+    import int4_weight_only_q4_gb300 as q4
+    w, x = synthetic.random_shape_problem(32, 256, 2, seed=3)
+    W = q4.QuantizedMatrix.from_packed(*q4.pack_host(w), device="cpu", tiled=False)
+    X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    ws = q4.Workspace(0, "cpu")
+    for fn in (lambda Y: q4.gemm_skinny(W, X, Y, workspace=ws), lambda Y: q4.gemm_skinny_noalloc(W, X, Y)):
+        with pytest.raises(ValueError, match="smaller than"):
+            fn(torch.empty((2, 31), dtype=torch.float32))
+        with pytest.raises(TypeError, match="float32"):
+            fn(torch.empty((2, 32), dtype=torch.float16))
+        with pytest.raises(TypeError, match="contiguous"):
+            fn(torch.empty((32, 2), dtype=torch.float32).t())
+    with pytest.raises(ValueError, match="K = 256"):
+        q4.gemm_skinny(W, X[:, :128].contiguous(), torch.empty((2, 32)), workspace=ws)
+    with pytest.raises(ValueError, match="smaller than"):
+        q4.gemv(W, X[0], torch.empty((31,), dtype=torch.float32), workspace=ws)
+    with pytest.raises(ValueError, match="smaller than"):
+        q4.decode_step([W, W], [X, X], [torch.empty((2, 32)), torch.empty((1, 32))], workspace=ws)
+    with pytest.raises(ValueError, match="same batch size"):
+        q4.decode_step([W, W], [X, X[:1].contiguous()], [torch.empty((2, 32))] * 2, workspace=ws)
+    with pytest.raises(ValueError, match="int32"):
+        q4.argmax(torch.empty((2, 32)), torch.empty((2,), dtype=torch.int64))
+
+
+def test_noalloc_host_checks_and_injected_launch_failure(monkeypatch):
+    """q4_gemm_skinny_noalloc validates on the host like the other entry points, refuses sizes beyond
+    its scratch, and reports an injected launch failure without touching CUDA."""
+    L = _lib.lib
+    m = _lib.q4_matrix(16, 16, 16, 10, 256)                     # no tiled copy
+    assert L.q4_gemm_skinny_noalloc(ctypes.byref(m), 16, 1, 16, None) == _lib.Q4_ERR_INVALID_ARG
+    m = _lib.q4_matrix(None, None, None, 10, 256, 16)
+    assert L.q4_gemm_skinny_noalloc(ctypes.byref(m), 16, 9, 16, None) == _lib.Q4_ERR_INVALID_ARG
+    assert L.q4_gemm_skinny_noalloc(ctypes.byref(m), 8, 1, 16, None) == _lib.Q4_ERR_MISALIGNED
+    big = _lib.q4_matrix(None, None, None, 10, 32384, 16)
+    assert L.q4_gemm_skinny_noalloc(ctypes.byref(big), 16, 8, 16, None) == _lib.Q4_ERR_WORKSPACE
+    monkeypatch.setenv("Q4_FAULT_INJECT", "launch")
+    assert L.q4_gemm_skinny_noalloc(ctypes.byref(m), 16, 1, 16, None) == _lib.Q4_ERR_CUDA

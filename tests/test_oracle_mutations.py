@@ -159,3 +159,31 @@ def test_argmax_last_tie_is_caught():
     last = lambda v: np.array([len(r) - 1 - int(np.argmax(r[::-1])) for r in np.atleast_2d(v)])
     assert last(y).tolist() != [1]
     assert oracle.argmax_first(y).tolist() == [1]
+
+
+def _ambiguous_reversed_sort(y_ref_row, abs_bound):
+    r = np.sort(np.asarray(y_ref_row, dtype=np.float64))[::-1]
+    return r.size > 1 and (r[-1] - r[-2]) <= abs_bound
+
+
+def _ambiguous_smallest_gap_anywhere(y_ref_row, abs_bound):
+    r = np.sort(np.asarray(y_ref_row, dtype=np.float64))
+    return r.size > 1 and float(np.min(np.diff(r))) <= abs_bound
+
+
+def _ambiguous_strict(y_ref_row, abs_bound):
+    r = np.sort(np.asarray(y_ref_row, dtype=np.float64))
+    return r.size > 1 and (r[-1] - r[-2]) < abs_bound
+
+
+@pytest.mark.parametrize("mutant", [lambda y, b: True, lambda y, b: False, _ambiguous_reversed_sort,
+                                    _ambiguous_smallest_gap_anywhere, _ambiguous_strict],
+                         ids=["always_true", "always_false", "reversed_sort", "smallest_gap_anywhere",
+                              "strict_bound"])
+def test_argmax_ambiguous_mistake_is_caught(monkeypatch, mutant):
+    """The pin of argmax_ambiguous (which decides whether the exact-argmax parity check may accept a
+    second index) fails for each plausible mistake in it."""
+    from test_oracle_pins import test_argmax_ambiguous_decides_by_the_top_two_gap as pin
+    monkeypatch.setattr(oracle, "argmax_ambiguous", mutant)
+    with pytest.raises(AssertionError):
+        pin()

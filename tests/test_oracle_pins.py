@@ -286,6 +286,45 @@ def test_argmax_first_on_ties():
     assert got.tolist() == want == [1, 0, 1]
 
 
+def _top2_gap_by_hand(row):
+    """Gap between the largest value and the largest of the others (one occurrence of the maximum
+    removed), found with two plain passes -- no sort."""
+    best = 0
+    for i, v in enumerate(row):
+        if v > row[best]:
+            best = i
+    second = None
+    for i, v in enumerate(row):
+        if i != best and (second is None or v > second):
+            second = v
+    return row[best] - second
+
+
+def test_argmax_ambiguous_decides_by_the_top_two_gap():
+    """argmax_ambiguous(y, bound) is True exactly when the two largest logits are at most `bound`
+    apart.  Hand cases pin the boundary (the gap equal to the bound counts as ambiguous), a
+    repeated maximum (gap 0), a single logit (never ambiguous), negative rows, and rows whose
+    closest pair is not the top two (a smallest-gap-anywhere mistake fails there); a reversed
+    sort, or an answer that is always True or always False, fails the hand cases."""
+    cases = [
+        ([1.0, 3.0, 2.75], 0.125, False), ([1.0, 3.0, 2.75], 0.25, True), ([1.0, 3.0, 2.75], 0.5, True),
+        ([2.0, 5.0, 5.0, 1.0], 0.0, True), ([7.0], 1e9, False),
+        ([-4.0, -1.0, -3.0], 1.5, False), ([-4.0, -1.0, -3.0], 2.0, True),
+        ([5.0, 0.0, 4.0, 4.0625], 0.5, False), ([5.0, 0.0, 4.0, 4.0625], 0.9375, True),
+        ([0.0, 10.0, 10.001, 3.0], 0.01, True), ([0.0, 10.0, 9.0, 3.0], 0.5, False),
+    ]
+    for row, bound, want in cases:
+        assert bool(oracle.argmax_ambiguous(np.array(row), bound)) == want, (row, bound)
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        row = rng.standard_normal(int(rng.integers(2, 40)))
+        if rng.random() < 0.3:
+            row[int(rng.integers(row.size))] = row.max()          # a repeated maximum
+        gap = _top2_gap_by_hand(row.tolist())
+        for bound in (0.0, gap * 0.5, gap, gap * 1.5):
+            assert bool(oracle.argmax_ambiguous(row, bound)) == (gap <= bound), (row, bound)
+
+
 def test_rel_err_metric():
     r = np.array([[1.0, -2.0, 0.0, 4.0]])
     assert oracle.rel_err(r, r) == 0.0
