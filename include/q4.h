@@ -245,6 +245,20 @@ q4_status q4_step_stream(const q4_matrix* mats, int n_mats, float* const* Y, int
                          const void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * q4_step_stream_readonly -- a measurement aid, not a computation: the read-only
+ * twin of q4_step_stream (the rumik-oss-1 write-up, "Step 7: why the GEMV was
+ * stuck": a copy of the GEMV that performs the same loads but no arithmetic shows
+ * whether memory or the instruction stream sets the speed).  Same arguments,
+ * same checks, same launch shape, the same weight records, activation words and
+ * group sums read through the same shared-memory ring in the same tile order,
+ * and the same Y stores -- but no unpack, no tensor-core product and no scale or
+ * minimum arithmetic.  The values written to Y are meaningless.  Its time over
+ * q4_step_stream's is the practical ceiling of the access pattern.
+ */
+q4_status q4_step_stream_readonly(const q4_matrix* mats, int n_mats, float* const* Y, int B,
+                                  const void* ws, size_t ws_bytes, void* stream);
+
+/*
  * q4_gemm_skinny_noalloc -- Y = W X exactly as the tile kernel computes it
  * (q4_step_prepare + q4_step_stream on a one-matrix list), for callers that
  * cannot allocate device memory and so cannot supply a workspace: code that

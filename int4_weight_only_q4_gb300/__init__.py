@@ -26,6 +26,7 @@ MAX_B = 8
 __all__ = ["GROUP", "MAX_B", "Q4Error", "QuantizedMatrix", "Workspace", "pack_host", "plan",
            "workspace_bytes", "decode_step_workspace_bytes", "tiled_bytes", "gemv", "gemm_skinny", "decode_step",
            "argmax", "device_status", "DecodeStepGraph", "step_workspace_bytes", "step_prepare", "step_stream",
+           "step_stream_readonly",
            "gemm_skinny_noalloc", "pack_int8_host", "Int8Head", "sample_topk", "gemm_prefill",
            "flash_decode", "flash_decode_workspace", "header_functions", "lib"]
 
@@ -296,6 +297,20 @@ def step_stream(mats, Ys, B: int, workspace: Workspace, stream=None) -> None:
     yp = (c_vp * n)(*[_ptr(y) for y in Ys])
     check(lib.q4_step_stream(arr, n, yp, B, workspace.ptr(), workspace.nbytes, _stream_ptr(stream)),
           "q4_step_stream")
+
+
+def step_stream_readonly(mats, Ys, B: int, workspace: Workspace, stream=None) -> None:
+    """Measurement aid: the read-only twin of step_stream (same loads and stores, no arithmetic;
+    the values it writes to Ys are meaningless)."""
+    n = len(mats)
+    if len(Ys) != n:
+        raise ValueError("one output tensor per matrix")
+    for y, m in zip(Ys, mats):
+        _check_y(y, B, m.N)
+    arr = (q4_matrix * n)(*[m.c_struct() for m in mats])
+    yp = (c_vp * n)(*[_ptr(y) for y in Ys])
+    check(lib.q4_step_stream_readonly(arr, n, yp, B, workspace.ptr(), workspace.nbytes, _stream_ptr(stream)),
+          "q4_step_stream_readonly")
 
 
 def argmax(Y: torch.Tensor, idx: torch.Tensor | None = None, stream=None) -> torch.Tensor:

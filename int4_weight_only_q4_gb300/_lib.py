@@ -78,6 +78,9 @@ lib.q4_step_prepare.restype = ctypes.c_int
 lib.q4_step_stream.argtypes = [ctypes.POINTER(q4_matrix), ctypes.c_int, ctypes.POINTER(c_vp), ctypes.c_int, c_vp,
                                ctypes.c_size_t, c_vp]
 lib.q4_step_stream.restype = ctypes.c_int
+lib.q4_step_stream_readonly.argtypes = [ctypes.POINTER(q4_matrix), ctypes.c_int, ctypes.POINTER(c_vp), ctypes.c_int,
+                                        c_vp, ctypes.c_size_t, c_vp]
+lib.q4_step_stream_readonly.restype = ctypes.c_int
 lib.q4_gemm_skinny_noalloc.argtypes = [ctypes.POINTER(q4_matrix), c_vp, ctypes.c_int, c_vp, c_vp]
 lib.q4_gemm_skinny_noalloc.restype = ctypes.c_int
 lib.q4_noalloc_scratch_bytes.argtypes = []

@@ -969,7 +969,12 @@ struct TileParams {
 
 constexpr int kItemQ = 16;  // per-warp queue of tiles requested but not yet computed (> S)
 
-template <int WARPS, int S, int BT>
+// RO: the read-only twin (a measurement aid): the same loads, the same ring, the same tile
+// schedule and the same stores, with the unpack, the mma and the scale/min arithmetic replaced by an
+// XOR of the loaded words -- the rate this access pattern allows when no arithmetic is done
+// (the rumik-oss-1 write-up, "Step 7": a twin of the GEMV that loads but does no maths told
+// memory-bound from compute-bound).  Its outputs carry no meaning.
+template <int WARPS, int S, int BT, bool RO = false>
 __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __grid_constant__ TileParams p) {
     static_assert(S >= 2 && S < kItemQ, "ring depth");
     extern __shared__ __align__(128) unsigned char smem[];
@@ -1105,6 +1110,14 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
         issue(prev);  // S - 1 records ahead, into the slot read one step ago
         prev = rd;
         rd = rd + kRecBytes == S * kRecBytes ? 0 : rd + kRecBytes;
+        if constexpr (RO) {
+            uint32_t v = qa.x ^ qa.y ^ qa.z ^ qa.w ^ qb.x ^ qb.y ^ qb.z ^ qb.w ^ sc.x ^ sc.y ^ sv.x ^ sv.y;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v ^= xv[j].x ^ xv[j].y ^ xv[j].z ^ xv[j].w;
+            acc[g & 3] = __uint_as_float(__float_as_uint(acc[g & 3]) ^ v);
+            xg += 16 * BT;
+            Sg += 8;
+        } else {
         float cc[4];
         group_dot_x4(qa, qb, xv, cc);
         const float Sx = __uint_as_float(sv.x), Sy = __uint_as_float(sv.y);
@@ -1120,6 +1133,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
         acc[3] = fmaf(mb, Sy, acc[3]);
         xg += 16 * BT;
         Sg += 8;
+        }
         if (++g < G) return true;
         const TileMat& m = p.m[mi];
         const float f0 = ld_dep_f32(m.fac + 2 * t), f1 = ld_dep_f32(m.fac + 2 * t + 1);
@@ -2451,7 +2465,7 @@ q4_status tiles_prepare(const Knobs& k, const q4_matrix* mats, int n, const uint
 }
 
 q4_status tiles_stream(const Knobs& k, const q4_matrix* mats, int n, float* const* Y, int B, const void* ws,
-                       bool independent, int dev, int sms, cudaStream_t stream) {
+                       bool independent, int dev, int sms, cudaStream_t stream, bool read_only = false) {
     const int bt = batch_tile(k, 5, B);
     const int per_launch = independent ? kMaxMats : 1;
     size_t off = 0;
@@ -2514,8 +2528,12 @@ q4_status tiles_stream(const Knobs& k, const q4_matrix* mats, int n, float* cons
         else
             tf = bt == 1 ? q4_tiles_ring_kernel<32, 4, 1> : bt == 2 ? q4_tiles_ring_kernel<32, 4, 2>
                : bt == 4 ? q4_tiles_ring_kernel<32, 4, 4> : q4_tiles_ring_kernel<32, 4, 8>;
-        const unsigned threads = static_cast<unsigned>(k.tw * 32);
-        const q4_status s = launch(tf, dev, static_cast<unsigned>(grid), threads, smem, stream, k.pdl, tp);
+        if (read_only)  // the twin exists for the default shape only
+            tf = bt == 1 ? q4_tiles_ring_kernel<32, 4, 1, true> : bt == 2 ? q4_tiles_ring_kernel<32, 4, 2, true>
+               : bt == 4 ? q4_tiles_ring_kernel<32, 4, 4, true> : q4_tiles_ring_kernel<32, 4, 8, true>;
+        const unsigned threads = static_cast<unsigned>((read_only ? 32 : k.tw) * 32);
+        const size_t smem_l = read_only ? static_cast<size_t>(32) * 4 * kRecBytes : smem;
+        const q4_status s = launch(tf, dev, static_cast<unsigned>(grid), threads, smem_l, stream, k.pdl, tp);
         if (s != Q4_OK) return s;
     }
     return Q4_OK;
@@ -2843,6 +2861,19 @@ extern "C" q4_status q4_step_stream(const q4_matrix* mats, int n_mats, float* co
         if (!aligned(Y[i], 4)) return Q4_ERR_MISALIGNED;
     }
     return tiles_stream(knobs(), mats, n_mats, Y, B, ws, true, dev, sms, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" q4_status q4_step_stream_readonly(const q4_matrix* mats, int n_mats, float* const* Y, int B,
+                                             const void* ws, size_t ws_bytes, void* stream) {
+    int dev = 0, sms = 0;
+    const q4_status s = check_step(mats, n_mats, B, ws, ws_bytes, &dev, &sms);
+    if (s != Q4_OK) return s;
+    if (!Y) return Q4_ERR_INVALID_ARG;
+    for (int i = 0; i < n_mats; ++i) {
+        if (!Y[i]) return Q4_ERR_INVALID_ARG;
+        if (!aligned(Y[i], 4)) return Q4_ERR_MISALIGNED;
+    }
+    return tiles_stream(knobs(), mats, n_mats, Y, B, ws, true, dev, sms, static_cast<cudaStream_t>(stream), true);
 }
 
 // ------------------------------------------------------------------ no-allocation variant

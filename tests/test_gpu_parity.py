@@ -523,3 +523,28 @@ def test_error_statuses_on_device(q4, monkeypatch):
     q4.device_status()
     torch.cuda.synchronize()
     assert oracle.rel_err(y.cpu().numpy()[None], oracle_rows(w, x)) <= TOL
+
+
+def test_read_only_twin_runs_the_same_launch(q4):
+    """The measurement twin of the step kernel takes the same arguments and checks, launches cleanly
+    on a decode-step list and leaves no device error; it touches only the outputs it is given."""
+    mats, xs, _ = _decode_mats(q4, 1, 2, base=70)
+    X = [bf16_tensor(x) for x in xs]
+    ws = q4.Workspace(q4.step_workspace_bytes([m.K for m in mats], 2))
+    pad = 256
+    bufs = [torch.full((2 * m.N + 2 * pad,), 12345.0, device="cuda") for m in mats]
+    Y = [b[pad:pad + 2 * m.N].view(2, m.N) for b, m in zip(bufs, mats)]
+    q4.step_prepare(mats, X, ws)
+    q4.step_stream_readonly(mats, Y, 2, ws)
+    torch.cuda.synchronize()
+    q4.device_status()
+    for b, m in zip(bufs, mats):
+        assert bool((b[:pad] == 12345.0).all()) and bool((b[pad + 2 * m.N:] == 12345.0).all())
+    Y2 = [torch.empty((2, m.N), device="cuda") for m in mats]
+    q4.step_stream(mats, Y2, 2, ws)            # the real kernel on the same prepared activations
+    torch.cuda.synchronize()
+    ref = [torch.empty_like(y) for y in Y2]
+    q4.decode_step(mats, X, ref)
+    torch.cuda.synchronize()
+    for a, b in zip(Y2, ref):
+        assert torch.equal(a, b)
