@@ -302,6 +302,31 @@ size_t q4_noalloc_scratch_bytes(void);
 q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* idx, void* stream);
 
 /*
+ * Argmax over a row-sharded head (one process per GPU, each holding a range of
+ * the head's rows; the full logits never leave their GPUs).  A rank's best
+ * logit per batch row is packed into one 64-bit key whose order is the
+ * q4_argmax_f32 rule over the whole row: bits 63..32 rank the value (NaN above
+ * every number, -0 equal to +0, larger above smaller), bits 31..0 hold the
+ * complement of the global row index (lower index above higher among equal
+ * values); the top bit is then flipped so that signed int64 order equals it.
+ * The largest key over all ranks -- one MAX all-reduce of B int64 values -- is
+ * the whole row's argmax.  (The pages run on one GPU; this is the plain
+ * reading of splitting a GEMV's output rows across GPUs and merging the
+ * per-GPU maxima.)
+ *
+ * q4_argmax_key_f32 -- keys[b] = the key of the best of Y[b, 0..N-1] (device
+ *   fp32 [B, N], 4-byte aligned), whose global row indices are index_base + n.
+ *   keys device int64 [B], 8-byte aligned.  1 <= B <= 65535, 1 <= N < 2^31,
+ *   0 <= index_base and index_base + N <= 2^32 - 1.
+ * q4_argmax_key_index -- idx[b] = the global row index held in keys[b]
+ *   (device int64 [B] -> device int32 [B]).
+ * Both: Q4_ERR_INVALID_ARG for null pointers or out-of-range sizes,
+ * Q4_ERR_MISALIGNED, Q4_ERR_CUDA for a failed launch.  Asynchronous on stream.
+ */
+q4_status q4_argmax_key_f32(const float* Y, int B, int64_t N, int64_t index_base, int64_t* keys, void* stream);
+q4_status q4_argmax_key_index(const int64_t* keys, int B, int32_t* idx, void* stream);
+
+/*
  * q4_gemm_prefill -- Y[m, :] = W X[m, :] for a prompt of M tokens (the rumik-oss-1
  * write-up, "Step 8: a prefill that stays int4": no dequantised copy of the
  * weights; each group is expanded in registers for the tensor cores and its

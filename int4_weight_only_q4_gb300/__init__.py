@@ -26,7 +26,7 @@ MAX_B = 8
 __all__ = ["GROUP", "MAX_B", "Q4Error", "QuantizedMatrix", "Workspace", "pack_host", "plan",
            "workspace_bytes", "decode_step_workspace_bytes", "tiled_bytes", "gemv", "gemm_skinny", "decode_step",
            "argmax", "device_status", "DecodeStepGraph", "step_workspace_bytes", "step_prepare", "step_stream",
-           "step_stream_readonly",
+           "step_stream_readonly", "argmax_keys", "argmax_key_index",
            "gemm_skinny_noalloc", "pack_int8_host", "Int8Head", "sample_topk", "gemm_prefill",
            "flash_decode", "flash_decode_workspace", "header_functions", "lib"]
 
@@ -326,6 +326,35 @@ def argmax(Y: torch.Tensor, idx: torch.Tensor | None = None, stream=None) -> tor
     return idx
 
 
+def argmax_keys(Y: torch.Tensor, index_base: int = 0, keys: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Per batch row of fp32 logits [B, N] whose rows are global rows index_base.., the best one as a
+    64-bit key (q4_argmax_key_f32): the largest key over several row slices is the argmax of the
+    whole row."""
+    if Y.dtype != torch.float32 or not Y.is_contiguous():
+        raise TypeError("logits must be a contiguous float32 CUDA tensor")
+    Y2 = Y if Y.dim() == 2 else Y.view(1, -1)
+    B, N = Y2.shape
+    if keys is None:
+        keys = torch.empty((B,), dtype=torch.int64, device=Y.device)
+    if keys.dtype != torch.int64 or not keys.is_contiguous() or keys.numel() < B:
+        raise ValueError("keys must be a contiguous int64 tensor of at least B elements")
+    check(lib.q4_argmax_key_f32(_ptr(Y2), B, N, int(index_base), _ptr(keys), _stream_ptr(stream)),
+          "q4_argmax_key_f32")
+    return keys
+
+
+def argmax_key_index(keys: torch.Tensor, idx: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The global row index held in each argmax key (q4_argmax_key_index), int32 [B]."""
+    if keys.dtype != torch.int64 or not keys.is_contiguous():
+        raise TypeError("keys must be a contiguous int64 CUDA tensor")
+    B = keys.numel()
+    if idx is None:
+        idx = torch.empty((B,), dtype=torch.int32, device=keys.device)
+    _check_i32(idx, B, "idx")
+    check(lib.q4_argmax_key_index(_ptr(keys), B, _ptr(idx), _stream_ptr(stream)), "q4_argmax_key_index")
+    return idx
+
+
 class Int8Head:
     """An int8 output head resident on the GPU (per-row fp16 scales, tiled copy of the codes):
     logits and/or their argmax per batch row in one call (q8_head)."""
@@ -471,7 +500,8 @@ class DecodeStepGraph:
     """
 
     def __init__(self, mats, B: int, X=None, Y=None, workspace: Workspace | None = None, device="cuda",
-                 with_argmax_of: int | None = None, independent: bool = True):
+                 with_argmax_of: int | None = None, independent: bool = True, after=None):
+        self.after = after  # optional: after(stream) enqueues more library calls into the same graph
         self.mats = list(mats)
         self.B = B
         self.independent = independent
@@ -502,6 +532,8 @@ class DecodeStepGraph:
         decode_step(self.mats, self.X, self.Y, self.ws, stream=stream, independent=self.independent)
         if self.argmax_of is not None:
             argmax(self.Y[self.argmax_of], self.idx, stream=stream)
+        if self.after is not None:
+            self.after(stream)
 
     def replay(self):
         self.graph.replay()

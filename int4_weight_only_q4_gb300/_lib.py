@@ -89,6 +89,10 @@ lib.q4_device_status.argtypes = [c_vp]
 lib.q4_device_status.restype = ctypes.c_int
 lib.q4_argmax_f32.argtypes = [c_vp, ctypes.c_int, c_i64, c_vp, c_vp]
 lib.q4_argmax_f32.restype = ctypes.c_int
+lib.q4_argmax_key_f32.argtypes = [c_vp, ctypes.c_int, c_i64, c_i64, c_vp, c_vp]
+lib.q4_argmax_key_f32.restype = ctypes.c_int
+lib.q4_argmax_key_index.argtypes = [c_vp, ctypes.c_int, c_vp, c_vp]
+lib.q4_argmax_key_index.restype = ctypes.c_int
 lib.q8_pack_host.argtypes = [c_vp, c_i64, c_i64, c_vp, c_vp, ctypes.c_int]
 lib.q8_pack_host.restype = ctypes.c_int
 lib.q8_tiled_bytes.argtypes = [c_i64, c_i64]

@@ -1651,6 +1651,67 @@ __device__ __forceinline__ uint32_t rank_key(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// ================================================================== argmax keys (row-sharded heads)
+// The best logit of a row slice as one 64-bit key that orders like the argmax rule over the whole
+// row: bits 63..32 the value's rank_key, bits 31..0 the complement of its global index (a lower
+// index ranks higher among equal values).  Stored with the top bit flipped, so that signed 64-bit
+// order -- what a MAX all-reduce of int64 compares -- equals that unsigned order.  The best key of
+// several slices is the largest; its low 32 bits, complemented, are the global index.
+__device__ __forceinline__ uint64_t argmax_key(float v, uint32_t gidx) {
+    return (static_cast<uint64_t>(rank_key(v)) << 32) | static_cast<uint64_t>(~gidx);
+}
+
+// One CTA per row, the row read as in q4_argmax_kernel (16-byte words, scalar head and tail); the
+// largest key wins, so the visiting order does not matter.
+__global__ void __launch_bounds__(1024) q4_argmax_key_kernel(const float* __restrict__ Y, int N, uint32_t base,
+                                                             int64_t* keys) {
+    grid_dependency_wait();
+    const float* row = Y + static_cast<size_t>(blockIdx.x) * N;
+    uint64_t best = 0;
+    auto consider = [&](float v, int i) {
+        const uint64_t k = argmax_key(v, base + static_cast<uint32_t>(i));
+        best = k > best ? k : best;
+    };
+    const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(row) & 15u) >> 2);
+    const int head = min(N, (4 - mis) & 3);
+    const int n4 = (N - head) >> 2;
+    const int tail0 = head + 4 * n4;
+    const int tid = static_cast<int>(threadIdx.x);
+    if (tid < head) consider(ld_dep_f32(row + tid), tid);
+    if (tail0 + tid < N) consider(ld_dep_f32(row + tail0 + tid), tail0 + tid);
+    const float4* row4 = reinterpret_cast<const float4*>(row + head);
+    for (int j = tid; j < n4; j += 1024) {
+        const float4 v = ld_dep_f4(row4 + j);
+        const int i = head + 4 * j;
+        consider(v.x, i);
+        consider(v.y, i + 1);
+        consider(v.z, i + 2);
+        consider(v.w, i + 3);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t ok = __shfl_xor_sync(0xffffffffu, best, o);
+        best = ok > best ? ok : best;
+    }
+    __shared__ uint64_t sk[32];
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) sk[w] = best;
+    __syncthreads();
+    if (w == 0) {
+        best = threadIdx.x < (blockDim.x >> 5) ? sk[threadIdx.x] : 0;
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t ok = __shfl_xor_sync(0xffffffffu, best, o);
+            best = ok > best ? ok : best;
+        }
+        if (threadIdx.x == 0) keys[blockIdx.x] = static_cast<int64_t>(best ^ 0x8000000000000000ull);
+    }
+}
+
+__global__ void q4_argmax_key_index_kernel(const int64_t* __restrict__ keys, int B, int32_t* idx) {
+    grid_dependency_wait();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) idx[b] = static_cast<int32_t>(~static_cast<uint32_t>(static_cast<uint64_t>(keys[b])));
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(kSampleThreads) q4_sample_kernel(const float* Y, int N, int k, float inv_t,
                                                                    const float* noise, int32_t* token,
@@ -3158,6 +3219,26 @@ extern "C" q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* id
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, q4_argmax_kernel, Y, static_cast<int>(N), idx) == cudaSuccess ? Q4_OK
                                                                                                 : Q4_ERR_CUDA;
+}
+
+extern "C" q4_status q4_argmax_key_f32(const float* Y, int B, int64_t N, int64_t index_base, int64_t* keys,
+                                       void* stream) {
+    if (!Y || !keys || B < 1 || B > 65535 || N < 1 || N > 0x7fffffffLL) return Q4_ERR_INVALID_ARG;
+    if (index_base < 0 || index_base + N > 0xFFFFFFFFLL) return Q4_ERR_INVALID_ARG;
+    if (!aligned(Y, 4) || !aligned(keys, 8)) return Q4_ERR_MISALIGNED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4_ERR_CUDA;
+    return launch(q4_argmax_key_kernel, dev, static_cast<unsigned>(B), 1024u, 0, static_cast<cudaStream_t>(stream),
+                  env_int("Q4_PDL", 1) != 0, Y, static_cast<int>(N), static_cast<uint32_t>(index_base), keys);
+}
+
+extern "C" q4_status q4_argmax_key_index(const int64_t* keys, int B, int32_t* idx, void* stream) {
+    if (!keys || !idx || B < 1 || B > 65535) return Q4_ERR_INVALID_ARG;
+    if (!aligned(keys, 8) || !aligned(idx, 4)) return Q4_ERR_MISALIGNED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4_ERR_CUDA;
+    return launch(q4_argmax_key_index_kernel, dev, static_cast<unsigned>((B + 255) / 256), 256u, 0,
+                  static_cast<cudaStream_t>(stream), env_int("Q4_PDL", 1) != 0, keys, B, idx);
 }
 
 extern "C" q4_status q4_device_status(void* stream) {
