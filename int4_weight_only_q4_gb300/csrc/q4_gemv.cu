@@ -1981,6 +1981,350 @@ __global__ void __launch_bounds__(kSampleThreads) q4_sample_kernel(const float* 
     }
 }
 
+// ================================================================== top-k sampling over a CTA cluster
+// q4_sample_cluster_kernel: the same result as q4_sample_kernel for k <= kClusterMaxK, with each
+// row split over a cluster of kSC CTAs on kSC SMs (one row per cluster, grid (kSC, B)).
+// (1) CTA c takes chunk c of the row (ceil(N / kSC) rounded up to 4 elements) and finds its own
+// top min(k, chunk) by the argmax order, exactly: each thread keeps its 2 best keys; a two-pass
+// radix select (top 16 key bits) over those samples gives L, a lower bound of the k-th best key
+// in the chunk (the samples are chunk elements, so at least k elements reach it); every element
+// at or above L is gathered (one ballot per warp step) and the gathered 64-bit (key, ~index)
+// keys are ranked -- by counting when few, by a bitonic sort otherwise.  When more than
+// kSCCap elements reach L (long runs of equal values), an exact radix select over the chunk finds
+// the k-th best key T and its ties are taken lowest index first, as in q4_sample_kernel.
+// (2) After a cluster barrier the leader CTA copies every CTA's sorted list out of the others'
+// shared memory (distributed shared memory of this GPU's own SMs), a second barrier releases them,
+// and the leader ranks each candidate among all lists (its place in its own list plus, in every
+// other list, the number of larger keys, by binary search): ranks below k are the row's top k.
+// (3) Scores and the token as in q4_sample_kernel.  The row's top k is the union's top k because
+// every element of it is in its own chunk's top k; the 64-bit keys are unique, so every rank is.
+// No wait in this kernel spins: the two cluster barriers are hardware barriers that every thread
+// of every CTA of the cluster passes on every path.
+constexpr int kSC = 8;             // CTAs per row: one portable-size cluster
+constexpr int kSCThreads = 512;
+constexpr int kClusterMaxK = 128;  // larger k uses q4_sample_kernel
+constexpr int kSCCap = 2048;       // gathered chunk candidates held in shared memory
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 64-bit load from the shared memory of CTA `rank` of this cluster, at the offset `local` has here
+__device__ __forceinline__ unsigned long long ld_cluster_u64(const void* local, unsigned rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const float* Y, int N, int k, float inv_t,
+                                                                       const float* noise, int32_t* token,
+                                                                       int32_t* topk) {
+    __shared__ unsigned hist[256];
+    __shared__ unsigned long long cand[kSCCap];
+    __shared__ unsigned long long list[kClusterMaxK];       // this CTA's top min(k, len), best first
+    __shared__ unsigned long long all[kSC * kClusterMaxK];  // leader: every CTA's list
+    __shared__ unsigned long long fin[kClusterMaxK];        // leader: the row's top k, best first
+    __shared__ unsigned sh_prefix, sh_remain, sh_ties, sh_count, sh_tie_base;
+    __shared__ unsigned warp_sum[kSCThreads / 32];
+    __shared__ float best_s[kSCThreads / 32];
+    __shared__ int best_r[kSCThreads / 32];
+    grid_dependency_wait();  // the logits are usually the previous kernel's output
+    allow_dependents();
+    const int tid = static_cast<int>(threadIdx.x);
+    const int lane = tid & 31, warp = tid >> 5;
+    const unsigned crank = blockIdx.x;  // the cluster is the kSC CTAs of one blockIdx.y
+    const int b = static_cast<int>(blockIdx.y);
+    const float* row = Y + static_cast<size_t>(b) * N;
+    auto chunk_lo = [&](unsigned c) {
+        const long long chunk = ((static_cast<long long>(N) + kSC - 1) / kSC + 3) & ~3LL;
+        const long long v = static_cast<long long>(c) * chunk;
+        return static_cast<int>(v < N ? v : N);
+    };
+    const int lo = chunk_lo(crank);
+    const int len = chunk_lo(crank + 1) - lo;  // the last chunk ends at N (kSC chunks cover the row)
+    const int kc = k < len ? k : len;
+    constexpr int U = 4;
+    // fn(index, value) over this CTA's chunk; VEC: 16-byte words (the row is 16-byte aligned and N
+    // and every chunk start are multiples of 4)
+    auto for_chunk = [&](auto&& fn) {
+        if constexpr (VEC) {
+            const float4* c4 = reinterpret_cast<const float4*>(row + lo);
+            const int n4 = len >> 2;
+            for (int base = tid; base < n4; base += U * kSCThreads) {
+                float4 v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = base + u * kSCThreads;
+                    v[u] = j < n4 ? ld_dep_f4(c4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = base + u * kSCThreads;
+                    if (j < n4) {
+                        fn(lo + 4 * j, v[u].x);
+                        fn(lo + 4 * j + 1, v[u].y);
+                        fn(lo + 4 * j + 2, v[u].z);
+                        fn(lo + 4 * j + 3, v[u].w);
+                    }
+                }
+            }
+        } else {
+            for (int base = tid; base < len; base += U * kSCThreads) {
+                float v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = base + u * kSCThreads;
+                    v[u] = i < len ? ld_dep_f32(row + lo + i) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = base + u * kSCThreads;
+                    if (i < len) fn(lo + i, v[u]);
+                }
+            }
+        }
+    };
+    auto pack = [](uint32_t key, int i) {
+        return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
+    };
+    // one key into the radix histogram of this pass, one shared atomic per distinct bin of a warp
+    auto hist_add = [&](uint32_t key, uint32_t mask, uint32_t prefix, int shift) {
+        const bool in = (key & mask) == prefix;
+        const unsigned bin = (key >> shift) & 255u;
+        const unsigned act = __ballot_sync(__activemask(), in);
+        if (in) {
+            const unsigned peers = __match_any_sync(act, bin);
+            if (__ffs(peers) - 1 == lane) atomicAdd(&hist[bin], static_cast<unsigned>(__popc(peers)));
+        }
+    };
+    // warp 0: the digit whose bin holds the remain-th largest counted key, bins scanned from 255 down
+    // (lane l holds bins 255-8l .. 248-8l); writes sh_prefix, sh_remain (remain minus the keys in
+    // higher bins) and sh_ties (the keys in that bin)
+    auto select_digit = [&](uint32_t prefix, int shift, unsigned remain) {
+        if (warp != 0) return;
+        unsigned c[8], local = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c[j] = hist[255 - 8 * lane - j];
+            local += c[j];
+        }
+        unsigned incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const unsigned excl = incl - local;
+        if (excl < remain && remain <= incl) {
+            unsigned above = excl;
+            int j = 0;
+            for (; j < 7; ++j) {
+                if (above + c[j] >= remain) break;
+                above += c[j];
+            }
+            sh_prefix = prefix | (static_cast<uint32_t>(255 - 8 * lane - j) << shift);
+            sh_remain = remain - above;
+            sh_ties = c[j];
+        }
+    };
+    // radix select of the remain-th largest key among those fed by `feed` (top `passes` bytes)
+    auto radix = [&](int passes, unsigned remain, auto&& feed) {
+        uint32_t prefix = 0, mask = 0;
+        for (int pass = 0; pass < passes; ++pass) {
+            const int shift = 24 - 8 * pass;
+            if (tid < 256) hist[tid] = 0;
+            __syncthreads();
+            feed(mask, prefix, shift);
+            __syncthreads();
+            select_digit(prefix, shift, remain);
+            __syncthreads();
+            prefix = sh_prefix;
+            remain = sh_remain;
+            mask |= 0xFFu << shift;
+        }
+        return prefix;
+    };
+    // bitonic sort, descending, of a[0..P) (P a power of two) by the whole block
+    auto sort_desc = [&](unsigned long long* a, int P) {
+        for (int size = 2; size <= P; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < P; i += kSCThreads) {
+                    const int j = i ^ stride;
+                    if (j > i) {
+                        const bool desc = (i & size) == 0;
+                        const unsigned long long x = a[i], y = a[j];
+                        if (desc ? (x < y) : (x > y)) {
+                            a[i] = y;
+                            a[j] = x;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+    };
+
+    // ---- (1) this chunk's top kc, best first, into list[0..kc)
+    if (kc > 0) {
+        uint32_t t0 = 0u, t1 = 0u;  // the thread's two best keys (0 sorts below every element's key)
+        for_chunk([&](int, float v) {
+            const uint32_t key = rank_key(v);
+            if (key > t1) {
+                if (key > t0) { t1 = t0; t0 = key; }
+                else t1 = key;
+            }
+        });
+        if (tid == 0) sh_count = 0;
+        // L: the top 16 bits of the kc-th best sample, a lower bound of the chunk's kc-th best key
+        const uint32_t L = radix(2, static_cast<unsigned>(kc), [&](uint32_t mask, uint32_t prefix, int shift) {
+            hist_add(t0, mask, prefix, shift);
+            hist_add(t1, mask, prefix, shift);
+        });
+        for_chunk([&](int i, float v) {
+            const uint32_t key = rank_key(v);
+            const bool take = key >= L;
+            const unsigned act = __activemask();
+            const unsigned bal = __ballot_sync(act, take);
+            const int leader = __ffs(act) - 1;
+            unsigned base = 0;
+            if (lane == leader && bal) base = atomicAdd(&sh_count, static_cast<unsigned>(__popc(bal)));
+            base = __shfl_sync(act, base, leader);
+            if (take) {
+                const unsigned pos = base + __popc(bal & ((1u << lane) - 1u));
+                if (pos < static_cast<unsigned>(kSCCap)) cand[pos] = pack(key, i);
+            }
+        });
+        __syncthreads();
+        int M = static_cast<int>(sh_count);
+        if (M > kSCCap) {
+            // too many to hold: the exact kc-th best key T of the chunk, the keys above it, and of
+            // the keys equal to T the lowest-index ones
+            const uint32_t T = radix(4, static_cast<unsigned>(kc), [&](uint32_t mask, uint32_t prefix, int shift) {
+                for_chunk([&](int, float v) { hist_add(rank_key(v), mask, prefix, shift); });
+            });
+            const unsigned take_ties = sh_remain;
+            const unsigned above_T = static_cast<unsigned>(kc) - take_ties;
+            const bool all_ties = sh_ties == take_ties;
+            if (tid == 0) { sh_count = 0; sh_tie_base = 0; }
+            __syncthreads();
+            for_chunk([&](int i, float v) {
+                const uint32_t key = rank_key(v);
+                if (key > T) cand[atomicAdd(&sh_count, 1u)] = pack(key, i);
+                else if (key == T && all_ties) cand[above_T + atomicAdd(&sh_tie_base, 1u)] = pack(key, i);
+            });
+            if (!all_ties) {
+                // walk the chunk in index order, kSCThreads at a time; a block-wide exclusive scan
+                // gives each tie its rank among ties
+                __syncthreads();
+                unsigned running = 0;
+                for (int base = 0; base < len && running < take_ties; base += kSCThreads) {
+                    const int i = lo + base + tid;
+                    const unsigned flag = (base + tid < len && rank_key(ld_dep_f32(row + i)) == T) ? 1u : 0u;
+                    const unsigned bal = __ballot_sync(0xffffffffu, flag);
+                    if (lane == 0) warp_sum[warp] = __popc(bal);
+                    __syncthreads();
+                    unsigned before = 0, total = 0;
+                    for (int w = 0; w < kSCThreads / 32; ++w) {
+                        const unsigned c = warp_sum[w];
+                        if (w < warp) before += c;
+                        total += c;
+                    }
+                    const unsigned r = running + before + __popc(bal & ((1u << lane) - 1u));
+                    if (flag && r < take_ties) cand[above_T + r] = pack(T, i);
+                    running += total;
+                    __syncthreads();
+                }
+            }
+            __syncthreads();
+            M = kc;
+        }
+        if (M <= 256) {
+            // rank by counting: the keys are unique, so the ranks are a permutation
+            if (tid < M) {
+                const unsigned long long x = cand[tid];
+                int r = 0;
+                for (int j = 0; j < M; ++j) r += cand[j] > x ? 1 : 0;
+                if (r < kc) list[r] = x;
+            }
+        } else {
+            int P = 1;
+            while (P < M) P <<= 1;
+            for (int i = M + tid; i < P; i += kSCThreads) cand[i] = 0ull;
+            __syncthreads();
+            sort_desc(cand, P);
+            if (tid < kc) list[tid] = cand[tid];
+        }
+    }
+    __syncthreads();
+    cluster_barrier();  // every CTA's list is complete and visible to the cluster
+
+    // ---- (2) the leader merges the lists
+    auto list_len = [&](unsigned c) {
+        const int l = chunk_lo(c + 1) - chunk_lo(c);
+        return k < l ? k : l;
+    };
+    if (crank == 0) {
+        for (int t = tid; t < kSC * kClusterMaxK; t += kSCThreads) {
+            const unsigned c = static_cast<unsigned>(t / kClusterMaxK);
+            const int j = t % kClusterMaxK;
+            if (j < list_len(c)) all[t] = c == 0 ? list[j] : ld_cluster_u64(&list[j], c);
+        }
+    }
+    __syncthreads();
+    cluster_barrier();  // the others' shared memory is no longer read: they may exit
+    if (crank != 0) return;
+    for (int t = tid; t < kSC * kClusterMaxK; t += kSCThreads) {
+        const int c = t / kClusterMaxK, j = t % kClusterMaxK;
+        if (j >= list_len(c)) continue;
+        const unsigned long long x = all[t];
+        int r = j;
+        for (int o = 0; o < kSC; ++o) {
+            if (o == c) continue;
+            const unsigned long long* a = all + o * kClusterMaxK;
+            int l0 = 0, l1 = list_len(o);  // entries of list o above x: a[0..l0)
+            while (l0 < l1) {
+                const int mid = (l0 + l1) >> 1;
+                if (a[mid] > x) l0 = mid + 1;
+                else l1 = mid;
+            }
+            r += l0;
+        }
+        if (r < k) fin[r] = x;
+    }
+    __syncthreads();
+
+    // ---- (3) scores and the token
+    float s = -__int_as_float(0x7f800000);
+    int r = 0x7fffffff;
+    if (tid < k) {
+        const int my_idx = static_cast<int>(~static_cast<uint32_t>(fin[tid] & 0xFFFFFFFFull));
+        if (topk) topk[static_cast<size_t>(b) * k + tid] = my_idx;
+        const float v = ld_dep_f32(row + my_idx);
+        s = __fadd_rn(__fmul_rn(v, inv_t), ld_dep_f32(noise + static_cast<size_t>(b) * k + tid));
+        r = tid;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, s, o);
+        const int orr = __shfl_xor_sync(0xffffffffu, r, o);
+        if (ranks_above(os, orr, s, r)) { s = os; r = orr; }
+    }
+    if (lane == 0) { best_s[warp] = s; best_r[warp] = r; }
+    __syncthreads();
+    if (warp == 0) {
+        s = lane < kSCThreads / 32 ? best_s[lane] : -__int_as_float(0x7f800000);
+        r = lane < kSCThreads / 32 ? best_r[lane] : 0x7fffffff;
+        for (int o = 16; o > 0; o >>= 1) {
+            const float os = __shfl_xor_sync(0xffffffffu, s, o);
+            const int orr = __shfl_xor_sync(0xffffffffu, r, o);
+            if (ranks_above(os, orr, s, r)) { s = os; r = orr; }
+        }
+        if (lane == 0) token[b] = static_cast<int32_t>(~static_cast<uint32_t>(fin[r] & 0xFFFFFFFFull));
+    }
+}
+
 // ================================================================== int4 prefill GEMM
 // q4_prefill_kernel: Y[m, n] = sum_k w_hat[n, k] X[m, k] for a prompt of M tokens (the rumik-oss-1
 // write-up, "Step 8: a prefill that stays int4": no dequantised copy of the weights; each group is
@@ -3198,6 +3542,27 @@ extern "C" q4_status q4_sample_topk(const float* Y, int B, int64_t N, int k, flo
     if (cudaGetDevice(&dev) != cudaSuccess) return Q4_ERR_CUDA;
     const bool vec = aligned(Y, 16) && (N % 4) == 0;
     const Knobs kn = knobs();
+    if (k <= kClusterMaxK && env_int("Q4_SAMPLE_CLUSTER", 1) != 0) {
+        // one cluster of kSC CTAs per row
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(kSC, static_cast<unsigned>(B));
+        cfg.blockDim = dim3(kSCThreads);
+        cfg.stream = static_cast<cudaStream_t>(stream);
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = kn.pdl ? 1 : 0;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = kSC;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        auto cf = vec ? q4_sample_cluster_kernel<true> : q4_sample_cluster_kernel<false>;
+        return cudaLaunchKernelEx(&cfg, cf, Y, static_cast<int>(N), k, inv_temperature, noise, token, topk) ==
+                       cudaSuccess
+                   ? Q4_OK
+                   : Q4_ERR_CUDA;
+    }
     auto fn = vec ? q4_sample_kernel<true> : q4_sample_kernel<false>;
     return launch(fn, dev, static_cast<unsigned>(B), static_cast<unsigned>(kSampleThreads), 0,
                   static_cast<cudaStream_t>(stream), kn.pdl, Y, static_cast<int>(N), k, inv_temperature, noise, token,

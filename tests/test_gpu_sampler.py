@@ -90,3 +90,27 @@ def test_greedy_cases_match_argmax(q4):
     am = q4.argmax(Y)
     torch.cuda.synchronize()
     assert torch.equal(tok, am)
+
+
+@pytest.mark.parametrize("cluster", ["1", "0"])
+def test_each_kernel_on_every_candidate_path(q4, monkeypatch, cluster):
+    """k <= 128 runs one cluster of CTAs per row (Q4_SAMPLE_CLUSTER=0 forces the one-CTA kernel):
+    rows whose chunks gather few candidates (ranked by counting), hundreds (a bitonic sort) or more
+    than fit (the exact radix select with ordered ties), empty chunks of short rows, and rows that
+    do not start on a 16-byte boundary -- every one equal to the oracle."""
+    monkeypatch.setenv("Q4_SAMPLE_CLUSTER", cluster)
+    rng = np.random.default_rng(11)
+    cases = [
+        (rng.standard_normal((2, 65536)) * 3, 50),                      # few candidates per chunk
+        (rng.integers(0, 10, (2, 65536)), 50),                          # ~800 equal top values per chunk
+        (rng.integers(0, 3, (2, 65536)), 64),                           # more than fit: exact path
+        (np.zeros((2, 65536)), 128),                                    # one value everywhere
+        (rng.standard_normal((3, 33)), 33),                             # short rows: some chunks empty
+        (rng.standard_normal((2, 5)), 2),
+        (rng.standard_normal((2, 70001)), 128),                         # N not a multiple of 4
+        (np.round(rng.standard_normal((2, 65536)) * 2), 1),
+    ]
+    for i, (y, k) in enumerate(cases):
+        y = np.ascontiguousarray(y, dtype=np.float32)
+        check(q4, y, k, 1.25, seed=100 + i)
+        check(q4, y, k, 0.5, seed=200 + i, offset=1)
