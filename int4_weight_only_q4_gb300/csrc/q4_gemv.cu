@@ -1985,52 +1985,57 @@ __global__ void __launch_bounds__(kSampleThreads) q4_sample_kernel(const float* 
 // q4_sample_cluster_kernel: the same result as q4_sample_kernel for k <= kClusterMaxK, with each
 // row split over a cluster of kSC CTAs on kSC SMs (one row per cluster, grid (kSC, B)).
 // (1) CTA c takes chunk c of the row (ceil(N / kSC) rounded up to 4 elements) and finds its own
-// top min(k, chunk) by the argmax order, exactly: each thread keeps its 2 best keys; a two-pass
-// radix select (top 16 key bits) over those samples gives L, a lower bound of the k-th best key
-// in the chunk (the samples are chunk elements, so at least k elements reach it); every element
-// at or above L is gathered (one ballot per warp step) and the gathered 64-bit (key, ~index)
-// keys are ranked -- by counting when few, by a bitonic sort otherwise.  When more than
-// kSCCap elements reach L (long runs of equal values), an exact radix select over the chunk finds
-// the k-th best key T and its ties are taken lowest index first, as in q4_sample_kernel.
-// (2) After a cluster barrier the leader CTA copies every CTA's sorted list out of the others'
-// shared memory (distributed shared memory of this GPU's own SMs), a second barrier releases them,
-// and the leader ranks each candidate among all lists (its place in its own list plus, in every
-// other list, the number of larger keys, by binary search): ranks below k are the row's top k.
-// (3) Scores and the token as in q4_sample_kernel.  The row's top k is the union's top k because
-// every element of it is in its own chunk's top k; the 64-bit keys are unique, so every rank is.
-// No wait in this kernel spins: the two cluster barriers are hardware barriers that every thread
-// of every CTA of the cluster passes on every path.
+// top min(k, chunk) by the argmax order, exactly.  Each thread's best key is a sample; a two-pass
+// radix select over the top 16 bits of those samples gives L, a lower bound of the chunk's k-th
+// best key (the samples are chunk elements, so at least k elements reach it).  Every element at
+// or above L is gathered (a count per thread, one scan and one shared atomic per warp) and the
+// gathered 64-bit (key, ~index) keys are ranked -- by counting when few, by a bitonic sort
+// otherwise.  When more than kSCCap elements reach L (long runs of equal values), an exact radix
+// select over the chunk finds the k-th best key T and its ties are taken lowest index first, as
+// in q4_sample_kernel.  The CTA writes its sorted list into the leader CTA's shared memory
+// (distributed shared memory of this GPU's own SMs), padded with zero keys.
+// (2) One cluster barrier; the other CTAs leave.  The leader ranks each entry among all lists (its
+// place in its own list plus, in every other list, the number of larger keys, by binary search):
+// the entries ranked below k are the row's top k, each scored where it is ranked.
+// (3) Scores and the token as in q4_sample_kernel; the logit comes back from its key.
+// The row's top k is the union's top k because every element of it is in its own chunk's top k;
+// the 64-bit keys are unique, so every rank is.  No wait in this kernel spins: the cluster
+// barrier is a hardware barrier that every thread of every CTA of the cluster reaches on every
+// path.
 constexpr int kSC = 8;             // CTAs per row: one portable-size cluster
-constexpr int kSCThreads = 512;
+constexpr int kSCThreads = 1024;
 constexpr int kClusterMaxK = 128;  // larger k uses q4_sample_kernel
 constexpr int kSCCap = 2048;       // gathered chunk candidates held in shared memory
+constexpr int kSCRegs = 8;         // keys per thread held in registers when the chunk fits
+constexpr int kListStride = kClusterMaxK + 1;  // lists one 8-byte word apart in bank order
 
 __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 64-bit load from the shared memory of CTA `rank` of this cluster, at the offset `local` has here
-__device__ __forceinline__ unsigned long long ld_cluster_u64(const void* local, unsigned rank) {
+// 64-bit store into the shared memory of CTA `rank` of this cluster, at the offset `local` has here
+__device__ __forceinline__ void st_cluster_u64(void* local, unsigned rank, unsigned long long v) {
     uint32_t ra;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
-    unsigned long long v;
-    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(ra) : "memory");
-    return v;
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(ra), "l"(v) : "memory");
 }
 
-template <bool VEC>
+// VEC: 16-byte loads (row 16-byte aligned, N a multiple of 4); REG: the chunk's keys fit in
+// registers (kSCThreads * kSCRegs) and the row is read once
+template <bool VEC, bool REG>
 __global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const float* Y, int N, int k, float inv_t,
                                                                        const float* noise, int32_t* token,
                                                                        int32_t* topk) {
-    __shared__ unsigned hist[256];
+    __shared__ unsigned hist[2][256];
     __shared__ unsigned long long cand[kSCCap];
-    __shared__ unsigned long long list[kClusterMaxK];       // this CTA's top min(k, len), best first
-    __shared__ unsigned long long all[kSC * kClusterMaxK];  // leader: every CTA's list
-    __shared__ unsigned long long fin[kClusterMaxK];        // leader: the row's top k, best first
+    __shared__ unsigned long long all[kSC * kListStride];  // every CTA's list, list c at c * kListStride
+    __shared__ float s_noise[kClusterMaxK];
     __shared__ unsigned sh_prefix, sh_remain, sh_ties, sh_count, sh_tie_base;
     __shared__ unsigned warp_sum[kSCThreads / 32];
-    __shared__ float best_s[kSCThreads / 32];
-    __shared__ int best_r[kSCThreads / 32];
+    __shared__ unsigned long long my_best;            // this CTA's best (score, rank) key
+    __shared__ int my_idx[kClusterMaxK];              // this CTA's row index of each of its ranks
+    __shared__ unsigned long long cl_best[kSC];       // leader: every CTA's best key
+    __shared__ unsigned long long cl_idx[kSC];        // leader: the row index of each CTA's best
     grid_dependency_wait();  // the logits are usually the previous kernel's output
     allow_dependents();
     const int tid = static_cast<int>(threadIdx.x);
@@ -2038,21 +2043,58 @@ __global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const flo
     const unsigned crank = blockIdx.x;  // the cluster is the kSC CTAs of one blockIdx.y
     const int b = static_cast<int>(blockIdx.y);
     const float* row = Y + static_cast<size_t>(b) * N;
-    auto chunk_lo = [&](unsigned c) {
-        const long long chunk = ((static_cast<long long>(N) + kSC - 1) / kSC + 3) & ~3LL;
+    const int chunk = static_cast<int>(((static_cast<long long>(N) + kSC - 1) / kSC + 3) & ~3LL);
+    auto chunk_lo = [&](int c) {
         const long long v = static_cast<long long>(c) * chunk;
         return static_cast<int>(v < N ? v : N);
     };
-    const int lo = chunk_lo(crank);
-    const int len = chunk_lo(crank + 1) - lo;  // the last chunk ends at N (kSC chunks cover the row)
+    const int lo = chunk_lo(static_cast<int>(crank));
+    const int len = chunk_lo(static_cast<int>(crank) + 1) - lo;  // the last chunk ends at N
     const int kc = k < len ? k : len;
-    constexpr int U = 4;
-    // fn(index, value) over this CTA's chunk; VEC: 16-byte words (the row is 16-byte aligned and N
-    // and every chunk start are multiples of 4)
-    auto for_chunk = [&](auto&& fn) {
+    const int n4 = len >> 2;
+    if (tid < k) s_noise[tid] = ld_dep_f32(noise + static_cast<size_t>(b) * k + tid);
+    if (tid < 512) (&hist[0][0])[tid] = 0u;
+    if (tid == 0) {
+        sh_count = 0u;
+        my_best = 0ull;  // below every (score, rank) key
+    }
+    uint32_t rk[REG ? kSCRegs : 1];  // REG: the keys of this thread's elements (0 where none)
+    if constexpr (REG) {
         if constexpr (VEC) {
             const float4* c4 = reinterpret_cast<const float4*>(row + lo);
-            const int n4 = len >> 2;
+#pragma unroll
+            for (int u = 0; u < kSCRegs / 4; ++u) {
+                const int j = tid + u * kSCThreads;
+                const float4 x = j < n4 ? ld_dep_f4(c4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                rk[4 * u] = j < n4 ? rank_key(x.x) : 0u;
+                rk[4 * u + 1] = j < n4 ? rank_key(x.y) : 0u;
+                rk[4 * u + 2] = j < n4 ? rank_key(x.z) : 0u;
+                rk[4 * u + 3] = j < n4 ? rank_key(x.w) : 0u;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kSCRegs; ++u) {
+                const int i = tid + u * kSCThreads;
+                rk[u] = i < len ? rank_key(ld_dep_f32(row + lo + i)) : 0u;
+            }
+        }
+    }
+    constexpr int U = 4;
+    // fn(index, key) over this CTA's chunk
+    auto for_keys = [&](auto&& fn) {
+        if constexpr (REG) {
+#pragma unroll
+            for (int u = 0; u < kSCRegs; ++u) {
+                if constexpr (VEC) {
+                    const int j = tid + (u >> 2) * kSCThreads;
+                    if (j < n4) fn(lo + 4 * j + (u & 3), rk[u]);
+                } else {
+                    const int i = tid + u * kSCThreads;
+                    if (i < len) fn(lo + i, rk[u]);
+                }
+            }
+        } else if constexpr (VEC) {
+            const float4* c4 = reinterpret_cast<const float4*>(row + lo);
             for (int base = tid; base < n4; base += U * kSCThreads) {
                 float4 v[U];
 #pragma unroll
@@ -2064,10 +2106,10 @@ __global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const flo
                 for (int u = 0; u < U; ++u) {
                     const int j = base + u * kSCThreads;
                     if (j < n4) {
-                        fn(lo + 4 * j, v[u].x);
-                        fn(lo + 4 * j + 1, v[u].y);
-                        fn(lo + 4 * j + 2, v[u].z);
-                        fn(lo + 4 * j + 3, v[u].w);
+                        fn(lo + 4 * j, rank_key(v[u].x));
+                        fn(lo + 4 * j + 1, rank_key(v[u].y));
+                        fn(lo + 4 * j + 2, rank_key(v[u].z));
+                        fn(lo + 4 * j + 3, rank_key(v[u].w));
                     }
                 }
             }
@@ -2082,7 +2124,7 @@ __global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const flo
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int i = base + u * kSCThreads;
-                    if (i < len) fn(lo + i, v[u]);
+                    if (i < len) fn(lo + i, rank_key(v[u]));
                 }
             }
         }
@@ -2090,25 +2132,15 @@ __global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const flo
     auto pack = [](uint32_t key, int i) {
         return (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(i));
     };
-    // one key into the radix histogram of this pass, one shared atomic per distinct bin of a warp
-    auto hist_add = [&](uint32_t key, uint32_t mask, uint32_t prefix, int shift) {
-        const bool in = (key & mask) == prefix;
-        const unsigned bin = (key >> shift) & 255u;
-        const unsigned act = __ballot_sync(__activemask(), in);
-        if (in) {
-            const unsigned peers = __match_any_sync(act, bin);
-            if (__ffs(peers) - 1 == lane) atomicAdd(&hist[bin], static_cast<unsigned>(__popc(peers)));
-        }
-    };
-    // warp 0: the digit whose bin holds the remain-th largest counted key, bins scanned from 255 down
-    // (lane l holds bins 255-8l .. 248-8l); writes sh_prefix, sh_remain (remain minus the keys in
-    // higher bins) and sh_ties (the keys in that bin)
-    auto select_digit = [&](uint32_t prefix, int shift, unsigned remain) {
+    // warp 0: the digit whose bin of h holds the remain-th largest counted key, bins scanned from
+    // 255 down (lane l holds bins 255-8l .. 248-8l); writes sh_prefix (prefix | digit << shift),
+    // sh_remain (remain minus the keys in higher bins) and sh_ties (the keys in that bin)
+    auto select_digit = [&](const unsigned* h, uint32_t prefix, int shift, unsigned remain) {
         if (warp != 0) return;
         unsigned c[8], local = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            c[j] = hist[255 - 8 * lane - j];
+            c[j] = h[255 - 8 * lane - j];
             local += c[j];
         }
         unsigned incl = local;
@@ -2130,23 +2162,6 @@ __global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const flo
             sh_ties = c[j];
         }
     };
-    // radix select of the remain-th largest key among those fed by `feed` (top `passes` bytes)
-    auto radix = [&](int passes, unsigned remain, auto&& feed) {
-        uint32_t prefix = 0, mask = 0;
-        for (int pass = 0; pass < passes; ++pass) {
-            const int shift = 24 - 8 * pass;
-            if (tid < 256) hist[tid] = 0;
-            __syncthreads();
-            feed(mask, prefix, shift);
-            __syncthreads();
-            select_digit(prefix, shift, remain);
-            __syncthreads();
-            prefix = sh_prefix;
-            remain = sh_remain;
-            mask |= 0xFFu << shift;
-        }
-        return prefix;
-    };
     // bitonic sort, descending, of a[0..P) (P a power of two) by the whole block
     auto sort_desc = [&](unsigned long long* a, int P) {
         for (int size = 2; size <= P; size <<= 1) {
@@ -2166,52 +2181,101 @@ __global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const flo
             }
         }
     };
+    // this CTA's list goes to slots crank * kListStride .. of every CTA's `all`
+    unsigned long long* my_slots = all + crank * kListStride;
+    auto put = [&](int slot, unsigned long long v) {
+#pragma unroll
+        for (unsigned d = 0; d < kSC; ++d) {
+            if (d == crank) my_slots[slot] = v;
+            else st_cluster_u64(my_slots + slot, d, v);
+        }
+    };
 
-    // ---- (1) this chunk's top kc, best first, into list[0..kc)
+    // ---- (1) this chunk's top kc, best first, into the leader's shared memory
+    // Shared memory of another CTA may be written only once that CTA runs: the arrive here and the
+    // wait before the first such store let the cluster's start-up overlap the selection.
+    asm volatile("barrier.cluster.arrive.aligned;" ::: "memory");
+    int M = 0;
     if (kc > 0) {
-        uint32_t t0 = 0u, t1 = 0u;  // the thread's two best keys (0 sorts below every element's key)
-        for_chunk([&](int, float v) {
-            const uint32_t key = rank_key(v);
-            if (key > t1) {
-                if (key > t0) { t1 = t0; t0 = key; }
-                else t1 = key;
-            }
-        });
-        if (tid == 0) sh_count = 0;
-        // L: the top 16 bits of the kc-th best sample, a lower bound of the chunk's kc-th best key
-        const uint32_t L = radix(2, static_cast<unsigned>(kc), [&](uint32_t mask, uint32_t prefix, int shift) {
-            hist_add(t0, mask, prefix, shift);
-            hist_add(t1, mask, prefix, shift);
-        });
-        for_chunk([&](int i, float v) {
-            const uint32_t key = rank_key(v);
-            const bool take = key >= L;
-            const unsigned act = __activemask();
-            const unsigned bal = __ballot_sync(act, take);
-            const int leader = __ffs(act) - 1;
-            unsigned base = 0;
-            if (lane == leader && bal) base = atomicAdd(&sh_count, static_cast<unsigned>(__popc(bal)));
-            base = __shfl_sync(act, base, leader);
-            if (take) {
-                const unsigned pos = base + __popc(bal & ((1u << lane) - 1u));
-                if (pos < static_cast<unsigned>(kSCCap)) cand[pos] = pack(key, i);
-            }
-        });
+        uint32_t t0 = 0u;  // the thread's best key: its sample
+        for_keys([&](int, uint32_t key) { t0 = key > t0 ? key : t0; });
+        __syncthreads();  // histograms zeroed
+        atomicAdd(&hist[0][t0 >> 24], 1u);
         __syncthreads();
-        int M = static_cast<int>(sh_count);
-        if (M > kSCCap) {
-            // too many to hold: the exact kc-th best key T of the chunk, the keys above it, and of
-            // the keys equal to T the lowest-index ones
-            const uint32_t T = radix(4, static_cast<unsigned>(kc), [&](uint32_t mask, uint32_t prefix, int shift) {
-                for_chunk([&](int, float v) { hist_add(rank_key(v), mask, prefix, shift); });
+        select_digit(hist[0], 0u, 24, static_cast<unsigned>(kc));
+        __syncthreads();
+        if ((t0 >> 24) == (sh_prefix >> 24)) atomicAdd(&hist[1][(t0 >> 16) & 255u], 1u);
+        __syncthreads();
+        select_digit(hist[1], sh_prefix, 16, sh_remain);
+        __syncthreads();
+        // L: the top 16 bits of the kc-th best sample, a lower bound of the chunk's kc-th best key
+        const uint32_t L = sh_prefix;
+        if constexpr (REG) {
+            // this thread's elements at or above L; one warp scan and one shared atomic per warp
+            unsigned mine = 0;
+            for_keys([&](int, uint32_t key) { mine += key >= L ? 1u : 0u; });
+            if (__any_sync(0xffffffffu, mine != 0)) {
+                unsigned incl = mine;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                unsigned base = 0;
+                if (lane == 31) base = atomicAdd(&sh_count, incl);
+                unsigned pos = __shfl_sync(0xffffffffu, base, 31) + incl - mine;
+                if (mine)
+                    for_keys([&](int i, uint32_t key) {
+                        if (key >= L) {
+                            if (pos < static_cast<unsigned>(kSCCap)) cand[pos] = pack(key, i);
+                            ++pos;
+                        }
+                    });
+            }
+        } else {
+            for_keys([&](int i, uint32_t key) {
+                const bool take = key >= L;
+                const unsigned act = __activemask();
+                const unsigned bal = __ballot_sync(act, take);
+                const int leader = __ffs(act) - 1;
+                unsigned base = 0;
+                if (lane == leader && bal) base = atomicAdd(&sh_count, static_cast<unsigned>(__popc(bal)));
+                base = __shfl_sync(act, base, leader);
+                if (take) {
+                    const unsigned pos = base + __popc(bal & ((1u << lane) - 1u));
+                    if (pos < static_cast<unsigned>(kSCCap)) cand[pos] = pack(key, i);
+                }
             });
-            const unsigned take_ties = sh_remain;
+        }
+        __syncthreads();
+        M = static_cast<int>(sh_count);
+        if (M > kSCCap) {
+            // too many to hold: the exact kc-th best key T of the chunk (a four-pass radix select),
+            // the keys above it, and of the keys equal to T the lowest-index ones
+            uint32_t prefix = 0, mask = 0;
+            unsigned remain = static_cast<unsigned>(kc);
+            for (int pass = 0; pass < 4; ++pass) {
+                const int shift = 24 - 8 * pass;
+                if (tid < 256) hist[0][tid] = 0u;
+                __syncthreads();
+                for_keys([&](int, uint32_t key) {
+                    if ((key & mask) == prefix) atomicAdd(&hist[0][(key >> shift) & 255u], 1u);
+                });
+                __syncthreads();
+                select_digit(hist[0], prefix, shift, remain);
+                __syncthreads();
+                prefix = sh_prefix;
+                remain = sh_remain;
+                mask |= 0xFFu << shift;
+            }
+            const uint32_t T = prefix;
+            const unsigned take_ties = remain;
             const unsigned above_T = static_cast<unsigned>(kc) - take_ties;
             const bool all_ties = sh_ties == take_ties;
+            __syncthreads();
             if (tid == 0) { sh_count = 0; sh_tie_base = 0; }
             __syncthreads();
-            for_chunk([&](int i, float v) {
-                const uint32_t key = rank_key(v);
+            for_keys([&](int i, uint32_t key) {
                 if (key > T) cand[atomicAdd(&sh_count, 1u)] = pack(key, i);
                 else if (key == T && all_ties) cand[above_T + atomicAdd(&sh_tie_base, 1u)] = pack(key, i);
             });
@@ -2241,13 +2305,17 @@ __global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const flo
             __syncthreads();
             M = kc;
         }
+    }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster runs
+    if (tid >= kc && tid < kClusterMaxK) put(tid, 0ull);          // the padding
+    if (kc > 0) {
         if (M <= 256) {
             // rank by counting: the keys are unique, so the ranks are a permutation
             if (tid < M) {
                 const unsigned long long x = cand[tid];
                 int r = 0;
                 for (int j = 0; j < M; ++j) r += cand[j] > x ? 1 : 0;
-                if (r < kc) list[r] = x;
+                if (r < kc) put(r, x);
             }
         } else {
             int P = 1;
@@ -2255,73 +2323,65 @@ __global__ void __launch_bounds__(kSCThreads) q4_sample_cluster_kernel(const flo
             for (int i = M + tid; i < P; i += kSCThreads) cand[i] = 0ull;
             __syncthreads();
             sort_desc(cand, P);
-            if (tid < kc) list[tid] = cand[tid];
+            if (tid < kc) put(tid, cand[tid]);
         }
     }
-    __syncthreads();
-    cluster_barrier();  // every CTA's list is complete and visible to the cluster
+    cluster_barrier();  // every list is in every CTA's shared memory
 
-    // ---- (2) the leader merges the lists
-    auto list_len = [&](unsigned c) {
-        const int l = chunk_lo(c + 1) - chunk_lo(c);
-        return k < l ? k : l;
-    };
-    if (crank == 0) {
-        for (int t = tid; t < kSC * kClusterMaxK; t += kSCThreads) {
-            const unsigned c = static_cast<unsigned>(t / kClusterMaxK);
-            const int j = t % kClusterMaxK;
-            if (j < list_len(c)) all[t] = c == 0 ? list[j] : ld_cluster_u64(&list[j], c);
+    // ---- (2) each CTA ranks its own list's entries among all lists; (3) the entries ranked
+    // below k are scored in place, each CTA's best (a shared-memory 64-bit max) goes to the leader,
+    // and the best of those picks the token.
+    // Thread tid handles entry e = tid / kSC of this CTA's list against list o = tid % kSC: the
+    // entries of list o above it, by a branch-free binary search over the list's kClusterMaxK slots
+    // (steps 64 .. 1 count among the first 127, the last slot on its own; padding slots hold 0,
+    // below every key); the kSC lanes of an entry add their counts with shuffles.
+    static_assert(kSC * kClusterMaxK == kSCThreads, "one thread per (entry, list)");
+    {
+        const int e = tid / kSC, o = tid % kSC;
+        const unsigned long long x = my_slots[e];
+        const unsigned long long* a = all + o * kListStride;
+        int p = 0;
+#pragma unroll
+        for (int step = kClusterMaxK / 2; step > 0; step >>= 1) p += a[p + step - 1] > x ? step : 0;
+        p += a[p] > x ? 1 : 0;
+        int rank = o == static_cast<int>(crank) ? e : p;  // its own list: its place in it
+#pragma unroll
+        for (int d = kSC / 2; d > 0; d >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, d);
+        if (o == 0 && e < kc && rank < k) {
+            const int idx = static_cast<int>(~static_cast<uint32_t>(x & 0xFFFFFFFFull));
+            if (topk) topk[static_cast<size_t>(b) * k + rank] = idx;
+            // the logit back from its key (rank_key inverted; -0 comes back as +0 and every NaN as
+            // one NaN, which changes no comparison below)
+            const uint32_t key = static_cast<uint32_t>(x >> 32);
+            const float v = __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+            const float sc = __fadd_rn(__fmul_rn(v, inv_t), s_noise[rank]);
+            // the score's key above, the complemented rank below: the largest is the best score,
+            // NaN first, the lower rank among equal scores (the q4_sample_kernel rule)
+            const unsigned long long sk =
+                (static_cast<unsigned long long>(rank_key(sc)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(rank));
+            my_idx[rank] = idx;
+            atomicMax(&my_best, sk);
         }
     }
     __syncthreads();
-    cluster_barrier();  // the others' shared memory is no longer read: they may exit
-    if (crank != 0) return;
-    for (int t = tid; t < kSC * kClusterMaxK; t += kSCThreads) {
-        const int c = t / kClusterMaxK, j = t % kClusterMaxK;
-        if (j >= list_len(c)) continue;
-        const unsigned long long x = all[t];
-        int r = j;
-        for (int o = 0; o < kSC; ++o) {
-            if (o == c) continue;
-            const unsigned long long* a = all + o * kClusterMaxK;
-            int l0 = 0, l1 = list_len(o);  // entries of list o above x: a[0..l0)
-            while (l0 < l1) {
-                const int mid = (l0 + l1) >> 1;
-                if (a[mid] > x) l0 = mid + 1;
-                else l1 = mid;
-            }
-            r += l0;
+    if (tid == 0) {
+        const unsigned long long best = my_best;
+        const unsigned long long bidx =
+            best ? static_cast<unsigned long long>(my_idx[~static_cast<uint32_t>(best & 0xFFFFFFFFull)]) : 0ull;
+        if (crank == 0) {
+            cl_best[0] = best;
+            cl_idx[0] = bidx;
+        } else {
+            st_cluster_u64(&cl_best[crank], 0u, best);
+            st_cluster_u64(&cl_idx[crank], 0u, bidx);
         }
-        if (r < k) fin[r] = x;
     }
-    __syncthreads();
-
-    // ---- (3) scores and the token
-    float s = -__int_as_float(0x7f800000);
-    int r = 0x7fffffff;
-    if (tid < k) {
-        const int my_idx = static_cast<int>(~static_cast<uint32_t>(fin[tid] & 0xFFFFFFFFull));
-        if (topk) topk[static_cast<size_t>(b) * k + tid] = my_idx;
-        const float v = ld_dep_f32(row + my_idx);
-        s = __fadd_rn(__fmul_rn(v, inv_t), ld_dep_f32(noise + static_cast<size_t>(b) * k + tid));
-        r = tid;
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, s, o);
-        const int orr = __shfl_xor_sync(0xffffffffu, r, o);
-        if (ranks_above(os, orr, s, r)) { s = os; r = orr; }
-    }
-    if (lane == 0) { best_s[warp] = s; best_r[warp] = r; }
-    __syncthreads();
-    if (warp == 0) {
-        s = lane < kSCThreads / 32 ? best_s[lane] : -__int_as_float(0x7f800000);
-        r = lane < kSCThreads / 32 ? best_r[lane] : 0x7fffffff;
-        for (int o = 16; o > 0; o >>= 1) {
-            const float os = __shfl_xor_sync(0xffffffffu, s, o);
-            const int orr = __shfl_xor_sync(0xffffffffu, r, o);
-            if (ranks_above(os, orr, s, r)) { s = os; r = orr; }
-        }
-        if (lane == 0) token[b] = static_cast<int32_t>(~static_cast<uint32_t>(fin[r] & 0xFFFFFFFFull));
+    cluster_barrier();  // every CTA's best is in the leader's shared memory
+    if (crank == 0 && tid == 0) {
+        unsigned long long best = cl_best[0], bidx = cl_idx[0];
+        for (int c = 1; c < kSC; ++c)
+            if (cl_best[c] > best) { best = cl_best[c]; bidx = cl_idx[c]; }
+        token[b] = static_cast<int32_t>(bidx);
     }
 }
 
@@ -3557,7 +3617,9 @@ extern "C" q4_status q4_sample_topk(const float* Y, int B, int64_t N, int k, flo
         attr[1].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        auto cf = vec ? q4_sample_cluster_kernel<true> : q4_sample_cluster_kernel<false>;
+        const bool reg = (((N + kSC - 1) / kSC + 3) & ~int64_t{3}) <= int64_t{kSCThreads} * kSCRegs;
+        auto cf = vec ? (reg ? q4_sample_cluster_kernel<true, true> : q4_sample_cluster_kernel<true, false>)
+                      : (reg ? q4_sample_cluster_kernel<false, true> : q4_sample_cluster_kernel<false, false>);
         return cudaLaunchKernelEx(&cfg, cf, Y, static_cast<int>(N), k, inv_temperature, noise, token, topk) ==
                        cudaSuccess
                    ? Q4_OK
