@@ -727,7 +727,9 @@ def prefill_bench(q4, torch, mats, dev, args):
     W = next(m for m in mats if (m.N, m.K) == (25088, 3072))
     out = {}
     peak = json.load(open(PEAKS_FILE)).get("bf16_tflops") if os.path.exists(PEAKS_FILE) else None
+    kinds = {}
     for M in (128, 512):
+        kinds[M] = q4.prefill_kernel(W.K, M)
         X = torch.randn((M, W.K), device=dev).to(torch.bfloat16)
         Y = torch.empty((M, W.N), device=dev)
         ws = q4.Workspace(int(q4.lib.q4_prefill_workspace_bytes(W.K, M)), dev)
@@ -753,8 +755,12 @@ def prefill_bench(q4, torch, mats, dev, args):
         tf = 2 * M * W.N * W.K / (us * 1e-6) / 1e12
         out[f"m{M}"] = {"us_per_call": round(us, 2), "TFLOP/s": round(tf, 1),
                         "frac_of_bf16_peak": round(tf / peak, 4) if peak else None}
-    out["kernel"] = "q4_xprep_kernel + q4_prefill_kernel (mma.sync m16n8k16 bf16, fused 25088x3072)"
+    names = {"tcgen05": "q4_tc_prep_kernel + q4_prefill_tc_kernel (tcgen05.mma 128x128x16 bf16, TMEM "
+                        "accumulators, TMA activations; fused 25088x3072)",
+             "mma.sync": "q4_xprep_kernel + q4_prefill_kernel (mma.sync m16n8k16 bf16, fused 25088x3072)"}
+    out["kernel"] = "; ".join(sorted({f"M={m}: {names[k]}" for m, k in kinds.items()}))
     out["bound"] = "tensor"
+    out["peak_source"] = "measured bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
     return out
 
 

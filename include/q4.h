@@ -329,18 +329,29 @@ q4_status q4_argmax_key_index(const int64_t* keys, int B, int32_t* idx, void* st
 /*
  * q4_gemm_prefill -- Y[m, :] = W X[m, :] for a prompt of M tokens (the rumik-oss-1
  * write-up, "Step 8: a prefill that stays int4": no dequantised copy of the
- * weights; each group is expanded in registers for the tensor cores and its
- * scale and minimum are folded into the fp32 result).  fp32 accumulation; a tensor-core GEMM (mma.sync),
- * not bound by the weight bytes once M is large.
+ * weights; each group is expanded for the tensor cores and its scale and
+ * minimum are folded into the fp32 result).  fp32 accumulation; a tensor-core
+ * GEMM, not bound by the weight bytes once M is large.  Two kernels:
+ *   - on a compute capability 10.x device: tcgen05.mma with TMEM accumulators,
+ *     activations by TMA (a prep kernel first writes a scaled, slot-permuted
+ *     copy of X into the workspace), 128 x 128 output tiles;
+ *   - otherwise (or with the environment variable Q4_PREFILL_TC=0): mma.sync
+ *     over token blocks of 8.
+ *   Both are deterministic; they agree with each other to fp32 rounding.
  *   W   host pointer; W->tiled (device) is required.
  *   X   device bf16 bits [M, K], 16-byte aligned;  Y device fp32 [M, N].
- *   ws  device workspace of ws_bytes >= q4_prefill_workspace_bytes(K, M) (the
- *       prepared activations; no initial content needed).
+ *   ws  device workspace of ws_bytes >= q4_prefill_workspace_bytes(K, M) (enough
+ *       for either kernel; no initial content needed), 16-byte aligned.
  * Q4_ERR_INVALID_ARG for null pointers, no tiled copy or M outside 1..2^24.
+ * A bounded wait of the tcgen05 kernel that gives up is reported by
+ * q4_device_status as Q4_ERR_TIMEOUT.
+ * q4_prefill_kernel -- which kernel q4_gemm_prefill runs for (K, M) on the
+ *   current device: 1 the tcgen05 kernel, 0 the mma.sync kernel, -1 invalid sizes.
  */
 size_t q4_prefill_workspace_bytes(int64_t K, int64_t M);
 q4_status q4_gemm_prefill(const q4_matrix* W, const uint16_t* X, int64_t M, float* Y, void* ws, size_t ws_bytes,
                           void* stream);
+int q4_prefill_kernel(int64_t K, int64_t M);
 
 /*
  * q4_sample_topk -- top-k sampling with the Gumbel-max trick over logits

@@ -415,9 +415,18 @@ class Int8Head:
         return (Y if logits else None), (idx if argmax else None)
 
 
+def prefill_kernel(K: int, M: int) -> str:
+    """The kernel q4_gemm_prefill runs for (K, M) on the current device: "tcgen05" or "mma.sync"."""
+    k = int(lib.q4_prefill_kernel(K, M))
+    if k < 0:
+        raise ValueError(f"invalid prefill sizes K={K} M={M}")
+    return "tcgen05" if k == 1 else "mma.sync"
+
+
 def gemm_prefill(W: QuantizedMatrix, X: torch.Tensor, Y: torch.Tensor | None = None,
                  workspace: Workspace | None = None, stream=None) -> torch.Tensor:
-    """Y [M, N] = X [M, K] W^T for a prompt of M tokens (q4_gemm_prefill, tensor-core GEMM)."""
+    """Y [M, N] = X [M, K] W^T for a prompt of M tokens (q4_gemm_prefill, tensor-core GEMM; the
+    tcgen05 kernel for K <= 8192, see prefill_kernel)."""
     M = _check_x(X, W.K)
     X2 = X if X.dim() == 2 else X.view(1, -1)
     if Y is None:

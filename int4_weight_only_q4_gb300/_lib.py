@@ -109,6 +109,8 @@ lib.q4_prefill_workspace_bytes.argtypes = [c_i64, c_i64]
 lib.q4_prefill_workspace_bytes.restype = ctypes.c_size_t
 lib.q4_gemm_prefill.argtypes = [ctypes.POINTER(q4_matrix), c_vp, c_i64, c_vp, c_vp, ctypes.c_size_t, c_vp]
 lib.q4_gemm_prefill.restype = ctypes.c_int
+lib.q4_prefill_kernel.argtypes = [c_i64, c_i64]
+lib.q4_prefill_kernel.restype = ctypes.c_int
 lib.q4_flash_decode_chunks.argtypes = [ctypes.c_int, ctypes.c_int]
 lib.q4_flash_decode_chunks.restype = ctypes.c_int
 lib.q4_flash_decode_workspace_bytes.argtypes = [ctypes.c_int] * 5

@@ -1,8 +1,9 @@
 """Build libq4.so in-tree with nvcc for sm_103a (GB300).
 
-Three translation units (the GEMV/GEMM kernels, the attention kernels and the
-host packer) are compiled in parallel and linked into one shared library next to this file.  The CUDA
-runtime is linked statically, so the library needs only the NVIDIA driver.
+Four translation units (the GEMV/GEMM kernels, the attention kernels, the
+tensor-memory prefill GEMM and the host packer) are compiled in parallel and
+linked into one shared library next to this file.  The CUDA runtime is linked
+statically, so the library needs only the NVIDIA driver.
 """
 from __future__ import annotations
 
@@ -41,7 +42,7 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     nv = nvcc()
     extra = list(extra or [])
-    srcs = [("q4_gemv.cu", ARCH), ("q4_attn.cu", ARCH), ("q4_host.cpp", [])]
+    srcs = [("q4_gemv.cu", ARCH), ("q4_attn.cu", ARCH), ("q4_prefill_tc.cu", ARCH), ("q4_host.cpp", [])]
     objs = []
     cmds = []
     for name, arch in srcs:

@@ -3,7 +3,10 @@
 
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
+
+#include "q4.h"
 
 // D += A * B on the tensor cores: 16 x 8 x 16, bf16 operands, fp32 accumulators.
 static __device__ __forceinline__ void mma_bf16_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -114,9 +117,23 @@ static __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint
         : "memory");
 }
 
+// bf16 pair times m1 * m2 (powers of two), exact for the supported range (|x| < 2^121 after scaling).
+static __device__ __forceinline__ uint32_t bf16x2_scale(uint32_t v, float m1, float m2) {
+    const float lo = (__uint_as_float(v << 16) * m1) * m2, hi = (__uint_as_float(v & 0xFFFF0000u) * m1) * m2;
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Host side, defined in q4_gemv.cu.
 int q4i_sm_count(int* dev_out);  // SMs of the current device (cached), -1 on error
 bool q4i_fault_injected();       // Q4_FAULT_INJECT=launch: every launch reports Q4_ERR_CUDA
 // Defined in q4_attn.cu: read and clear the attention kernels' device error word (1 if a bounded
 // wait gave up since the last call, 0 if not, -1 if the read failed).
 int q4i_attn_take_error();
+// Defined in q4_prefill_tc.cu: the tensor-memory prefill GEMM (compute capability 10.x).
+bool q4i_prefill_tc_usable(int64_t K, int64_t M);
+size_t q4i_prefill_tc_ws(int64_t K, int64_t M);
+q4_status q4i_prefill_tc(const q4_matrix* W, const uint16_t* X, int64_t M, float* Y, void* ws, size_t ws_bytes,
+                         cudaStream_t stream, bool pdl);
+int q4i_prefill_take_error();  // as q4i_attn_take_error, for its error word

@@ -298,14 +298,6 @@ __device__ __forceinline__ void group_epilogue(float (&acc)[4], const float (&c)
     acc[3] = fmaf(mb, S.y, acc[3]);
 }
 
-// bf16 pair times m1 * m2 (powers of two), exact for the supported range (see stage_x).
-__device__ __forceinline__ uint32_t bf16x2_scale(uint32_t v, float m1, float m2) {
-    const float lo = (bf16lo_to_f32(v) * m1) * m2, hi = (bf16hi_to_f32(v) * m1) * m2;
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 // A block-wide barrier as a callable (stage_x takes the barrier of its caller).
 struct SyncThreads {
     __device__ void operator()() const { __syncthreads(); }
@@ -332,6 +324,20 @@ __device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0,
                                         float* fac, unsigned* colmax, int tid, int nthr, Sync sync) {
     const int items = Gs * B * 16;  // (local group, column, chunk t, word i); (t, i) fastest
     const int iters = (items + nthr - 1) / nthr;
+    // a thread's first two 16-byte pieces of x are loaded once, both up front, and kept for the
+    // second pass (one round trip to memory instead of up to four); later pieces are read twice
+    uint4 vk[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = it * nthr + tid;
+        vk[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < items) {
+            const int ti = idx & 15, gn = idx >> 4;
+            vk[it] = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(gn % B) * K +
+                                                     static_cast<size_t>(g0 + gn / B) * 128 + (ti >> 2) * 32 +
+                                                     (ti & 3) * 8);
+        }
+    }
     if (tid < 8) colmax[tid] = 0u;
     sync();
     for (int it = 0; it < iters; ++it) {
@@ -345,8 +351,8 @@ __device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0,
             n = gn % B;
             gl = gn / B;
             const int tt = ti >> 2, i = ti & 3;
-            const uint4 v = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(n) * K +
-                                                            static_cast<size_t>(g0 + gl) * 128 + tt * 32 + i * 8);
+            const uint4 v = it == 0 ? vk[0] : it == 1 ? vk[1] : *reinterpret_cast<const uint4*>(
+                x + static_cast<size_t>(n) * K + static_cast<size_t>(g0 + gl) * 128 + tt * 32 + i * 8);
             uint32_t mx = 0;
             const uint32_t h[8] = {v.x << 16, v.x & 0xFFFF0000u, v.y << 16, v.y & 0xFFFF0000u,
                                    v.z << 16, v.z & 0xFFFF0000u, v.w << 16, v.w & 0xFFFF0000u};
@@ -371,7 +377,7 @@ __device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0,
     for (int idx = tid; idx < Gs * 8; idx += nthr)
         if ((idx & 7) >= B) ssum[idx] = 0.f;
     sync();
-    for (int idx = tid; idx < items; idx += nthr) {
+    for (int it = 0, idx = tid; idx < items; ++it, idx += nthr) {
         const int ti = idx & 15;
         const int gn = idx >> 4;
         const int n = gn % B;
@@ -380,8 +386,8 @@ __device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0,
         const int e = static_cast<int>(colmax[n] >> 23) - 127;  // colmax == 0: e = -127
         int a = 120 - e;
         a = a < 6 ? 6 : (a > 253 ? 253 : a);
-        const uint4 v = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(n) * K +
-                                                        static_cast<size_t>(g0 + gl) * 128 + tt * 32 + i * 8);
+        const uint4 v = it == 0 ? vk[0] : it == 1 ? vk[1] : *reinterpret_cast<const uint4*>(
+            x + static_cast<size_t>(n) * K + static_cast<size_t>(g0 + gl) * 128 + tt * 32 + i * 8);
         // x * 2^a as two exact power-of-two products, so that 2^a itself need not be a float
         const int a1 = a > 127 ? 127 : a;
         const float m1 = __int_as_float((a1 + 127) << 23);
@@ -3401,7 +3407,13 @@ size_t prefill_ws(int64_t K, int64_t M) {
 
 extern "C" size_t q4_prefill_workspace_bytes(int64_t K, int64_t M) {
     if (K <= 0 || K % 128 != 0 || M < 1 || M > (1 << 24)) return 0;
-    return prefill_ws(K, M);
+    const size_t a = prefill_ws(K, M), b = q4i_prefill_tc_ws(K, M);  // enough for either kernel
+    return a > b ? a : b;
+}
+
+extern "C" int q4_prefill_kernel(int64_t K, int64_t M) {
+    if (K <= 0 || K % 128 != 0 || K > kMaxK || M < 1 || M > (1 << 24)) return -1;
+    return q4i_prefill_tc_usable(K, M) ? 1 : 0;
 }
 
 extern "C" q4_status q4_gemm_prefill(const q4_matrix* W, const uint16_t* X, int64_t M, float* Y, void* ws,
@@ -3410,7 +3422,8 @@ extern "C" q4_status q4_gemm_prefill(const q4_matrix* W, const uint16_t* X, int6
     q4_status st = check_shape(W->N, W->K);
     if (st != Q4_OK) return st;
     if (!aligned(W->tiled, 16) || !aligned(X, 16) || !aligned(Y, 4)) return Q4_ERR_MISALIGNED;
-    const size_t need = prefill_ws(W->K, M);
+    const bool tc = q4i_prefill_tc_usable(W->K, M);
+    const size_t need = tc ? q4i_prefill_tc_ws(W->K, M) : prefill_ws(W->K, M);
     if (!ws || ws_bytes < need) return Q4_ERR_WORKSPACE;
     if (!aligned(ws, 16)) return Q4_ERR_MISALIGNED;
     if (fault_injected()) return Q4_ERR_CUDA;
@@ -3418,6 +3431,8 @@ extern "C" q4_status q4_gemm_prefill(const q4_matrix* W, const uint16_t* X, int6
     if (device_sm_count(&dev) <= 0) return Q4_ERR_CUDA;
     const Knobs k = knobs();
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // on a tcgen05 device: the tensor-memory kernel (q4_prefill_tc.cu)
+    if (tc) return q4i_prefill_tc(W, X, M, Y, ws, ws_bytes, cs, k.pdl);
     const size_t stride = prep_bytes(W->K, 8);
     const size_t G = static_cast<size_t>(W->K / 128);
     const int64_t nblk = (M + 7) / 8;
@@ -3674,7 +3689,9 @@ extern "C" q4_status q4_device_status(void* stream) {
     if (cudaMemcpyFromSymbol(&v, g_q4_device_error, sizeof v) != cudaSuccess) return Q4_ERR_CUDA;
     const int attn = q4i_attn_take_error();
     if (attn < 0) return Q4_ERR_CUDA;
-    if (v == 0 && attn == 0) return Q4_OK;
+    const int pre = q4i_prefill_take_error();
+    if (pre < 0) return Q4_ERR_CUDA;
+    if (v == 0 && attn == 0 && pre == 0) return Q4_OK;
     if (v == 0) return Q4_ERR_TIMEOUT;
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_q4_device_error, &zero, sizeof zero) != cudaSuccess) return Q4_ERR_CUDA;

@@ -1,5 +1,9 @@
 """GPU parity of the int4 prefill GEMM (q4_gemm_prefill) against the fp64 CPU oracle.
 
+Two kernels serve the call: the tensor-memory kernel (tcgen05.mma, TMEM accumulators, TMA) on
+compute capability 10.x, and the mma.sync kernel elsewhere or when Q4_PREFILL_TC=0; both are
+checked.
+
 The rumik-oss-1 write-up's "Step 8: a prefill that stays int4": the prompt's M tokens multiply
 the int4 weights directly (no dequantised copy), on the tensor cores, with each group's scale and
 minimum folded into the fp32 result.  The oracle is the
@@ -36,16 +40,53 @@ def oracle_y(w, x, rows):
     return oracle.gemv_packed(p, sb, mb, x)
 
 
-@pytest.mark.parametrize("N,K", [(16, 128), (100, 1152), (1000, 640), (3072, 3072), (257, 8192)])
-@pytest.mark.parametrize("M", [1, 7, 8, 9, 64, 100, 130])
-def test_prefill_matches_oracle(q4, N, K, M):
+@pytest.mark.parametrize("path", ["tc", "mma"])
+@pytest.mark.parametrize("N,K", [(16, 128), (100, 1152), (1000, 640), (3072, 3072), (257, 8192), (64, 8320),
+                                 (40, 16384)])
+@pytest.mark.parametrize("M", [1, 7, 8, 9, 64, 100, 130, 300])
+def test_prefill_matches_oracle(q4, monkeypatch, path, N, K, M):
+    if path == "mma":
+        monkeypatch.setenv("Q4_PREFILL_TC", "0")
     w, x = synthetic.random_shape_problem(N, K, M, seed=N + M, outliers=True)
     W = q4.QuantizedMatrix.from_float(w)
     Y = q4.gemm_prefill(W, bf16_tensor(x))
     torch.cuda.synchronize()
     rows = np.arange(N) if N <= 1000 else np.random.default_rng(0).choice(N, 400, replace=False)
     e = oracle.rel_err(Y.cpu().numpy()[:, rows], oracle_y(w, x, rows))
-    assert e <= TOL, e
+    assert e <= TOL, (path, e)
+    q4.device_status()  # no bounded wait gave up
+
+
+def test_prefill_kernel_choice(q4, monkeypatch):
+    """On a compute capability 10.x device the tcgen05 kernel serves every shape; the
+    Q4_PREFILL_TC=0 switch selects the mma.sync kernel."""
+    if torch.cuda.get_device_capability()[0] == 10:
+        for K, M in ((3072, 512), (8192, 1), (65536, 3), (128, 1 << 24)):
+            assert q4.prefill_kernel(K, M) == "tcgen05", (K, M)
+    with pytest.raises(ValueError):
+        q4.prefill_kernel(100, 1)
+    monkeypatch.setenv("Q4_PREFILL_TC", "0")
+    assert q4.prefill_kernel(3072, 512) == "mma.sync"
+
+
+def test_prefill_kernels_agree_and_leave_rows_alone(q4, monkeypatch):
+    """Both kernels agree to fp32 rounding on a ragged shape (rows and tokens not multiples of the
+    128 x 128 tile), and neither writes outside Y (a guard band around it keeps its canaries)."""
+    N, K, M = 1000, 3072, 259
+    w, x = synthetic.random_shape_problem(N, K, M, seed=91, outliers=True)
+    W = q4.QuantizedMatrix.from_float(w)
+    X = bf16_tensor(x)
+    outs = []
+    for env in ("1", "0"):
+        monkeypatch.setenv("Q4_PREFILL_TC", env)
+        buf = torch.full((M * N + 2048,), 7.0, device="cuda")
+        Y = buf[1024:1024 + M * N].view(M, N)
+        q4.gemm_prefill(W, X, Y)
+        torch.cuda.synchronize()
+        assert bool((buf[:1024] == 7.0).all()) and bool((buf[1024 + M * N:] == 7.0).all()), env
+        outs.append(Y.clone())
+    assert torch.allclose(outs[0], outs[1], rtol=1e-4, atol=1e-5)
+    q4.device_status()
 
 
 def test_prefill_long_prompt_full_size(q4):
