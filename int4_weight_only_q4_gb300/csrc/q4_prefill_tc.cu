@@ -33,7 +33,7 @@
 //                (128 x 128 x 16, A from TMEM, B from shared memory) into accumulator buffer g % kDBufs,
 //                frees the A and B stages with tcgen05.commit, and signals the epilogue with another;
 //                it reads no memory between MMAs (a load would stall it until its MMAs drain) and
-//                learns that a step may go from a named barrier;
+//                learns that a group may go from a named barrier;
 //   warp 14      scheduler: waits on the mbarriers that gate a step and releases it to warp 1;
 //   warps 2..5   code expansion: thread = weight row 32 (w % 4) + lane; per group its 64 code bytes
 //                (loaded three groups ahead) become 64 TMEM columns (tcgen05.st) in a ring of
@@ -297,25 +297,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4_prefill_tc_kernel(const __gr
         // ---- MMA issue (one thread).  This warp reads no memory while its MMAs run: a load (shared or
         // global, by any lane, an mbarrier wait included) stalls the warp until its MMAs in flight have
         // drained, about 380 cycles each time.  The scheduler warp (14) does the waiting; the two warps
-        // meet at named barrier kStepBar once per half-group step (a strict rendezvous, so no step is
-        // skipped or taken twice), and the scheduler meets it at every step, also after a wait gave up,
-        // so this warp never blocks for good.
+        // meet at named barrier kStepBar once per group (a strict rendezvous, so no step is skipped or
+        // taken twice), and the scheduler meets it at every step, also after a wait gave up, so this
+        // warp never blocks for good.
         constexpr uint32_t idesc = tc_idesc(kTcRows, kTcTok);
         const uint64_t bd0 = sw128_desc(smem_addr(sB));
-        for (int h = 0; h < H; ++h) {
-            const int g = h >> 1, hf = h & 1, sa = h % kAStages, sb = h % kBStages;
+        for (int g = 0; g < G; ++g) {  // one step per group: its two half-groups, 8 MMAs
             asm volatile("bar.sync %0, 64;" ::"n"(kStepBar) : "memory");
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t d = tmem + static_cast<uint32_t>((g % kDBufs) * kTcTok);
-                const uint64_t bd = bd0 + static_cast<uint64_t>((sb * kSlotBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)  // K = 16 per instruction: 8 A columns, 32 bytes of each B row
-                    tc_mma_ta(d, tmemA + static_cast<uint32_t>(32 * sa + 8 * kk), bd + static_cast<uint64_t>(2 * kk),
-                              idesc, (hf | kk) != 0 ? 1u : 0u);
-                tc_commit(emptyA + sa);  // the stages are free once these MMAs have read them
-                tc_commit(emptyB + sb);
-                if (hf == 1) tc_commit(dfull + g % kDBufs);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int h = 2 * g + hf, sa = h % kAStages, sb = h % kBStages;
+                    const uint64_t bd = bd0 + static_cast<uint64_t>((sb * kSlotBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)  // K = 16 per instruction: 8 A columns, 32 bytes of each B row
+                        tc_mma_ta(d, tmemA + static_cast<uint32_t>(32 * sa + 8 * kk), bd + static_cast<uint64_t>(2 * kk),
+                                  idesc, (hf | kk) != 0 ? 1u : 0u);
+                    tc_commit(emptyA + sa);  // the stages are free once these MMAs have read them
+                    tc_commit(emptyB + sb);
+                }
+                tc_commit(dfull + g % kDBufs);
             }
             __syncwarp();
         }
@@ -326,17 +329,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4_prefill_tc_kernel(const __gr
         }
         __syncwarp();
     } else if (warp == 14) {
-        // ---- scheduler: per half-group step, the accumulator buffer is free (first half), the codes are
-        // in TMEM and the activations have landed; then the MMA warp may issue the step
+        // ---- scheduler: per group, the accumulator buffer is free, both half-groups' codes are in TMEM
+        // and their activations have landed; then the MMA warp may issue the group
         bool aborted = false;
-        for (int h = 0; h < H; ++h) {
-            const int g = h >> 1, sa = h % kAStages, sb = h % kBStages;
+        for (int g = 0; g < G; ++g) {
             if (!aborted) {  // after a wait gave up, the remaining steps go on garbage (the error word is set)
-                bool ok = true;
-                if ((h & 1) == 0)
-                    ok = tc_wait_warp(dempty + g % kDBufs, (static_cast<uint32_t>(g / kDBufs) & 1u) ^ 1u, abort_flag);
-                ok = ok && tc_wait_warp(fullA + sa, static_cast<uint32_t>(h / kAStages) & 1u, abort_flag) &&
-                     tc_wait_warp(fullB + sb, static_cast<uint32_t>(h / kBStages) & 1u, abort_flag);
+                bool ok = tc_wait_warp(dempty + g % kDBufs, (static_cast<uint32_t>(g / kDBufs) & 1u) ^ 1u, abort_flag);
+                for (int hf = 0; hf < 2 && ok; ++hf) {
+                    const int h = 2 * g + hf;
+                    ok = tc_wait_warp(fullA + h % kAStages, static_cast<uint32_t>(h / kAStages) & 1u, abort_flag) &&
+                         tc_wait_warp(fullB + h % kBStages, static_cast<uint32_t>(h / kBStages) & 1u, abort_flag);
+                }
                 aborted = !ok;
             }
             asm volatile("bar.sync %0, 64;" ::"n"(kStepBar) : "memory");
