@@ -874,7 +874,9 @@ def run_profile_small(args) -> int:
     """Small cases for ncu: `--profile-head8` one int8-head call (65,536 x 3072, seeded random codes on
     the device, B = --profile-batch, logits + argmax) after two warm-up calls; `--profile-sampler`
     one top-k (k = 50) Gumbel-max sampling call over 65,536 logits after two warm-up calls;
-    `--profile-attn` three flash-decoding calls, batch --profile-batch over an 8,192-position cache."""
+    `--profile-attn` three flash-decoding calls, batch --profile-batch over an 8,192-position cache;
+    `--profile-prefill M` three prefill GEMM calls of M tokens on a 25,088 x 3072 matrix with seeded
+    random codes (the fused projection's shape)."""
     import torch
     import int4_weight_only_q4_gb300 as q4
     dev = torch.device("cuda", 0)
@@ -889,6 +891,16 @@ def run_profile_small(args) -> int:
         X = torch.randn((B, K), device=dev, generator=gen).to(torch.bfloat16)
         for _ in range(3):
             Y, idx = H(X)
+    elif args.profile_prefill:
+        Np, Kp, _ = synthetic.SHAPES["fused"]
+        W = q4.QuantizedMatrix(torch.randint(0, 256, (Np, Kp // 2), dtype=torch.uint8, device=dev, generator=gen),
+                               (torch.rand((Np, Kp // 128), device=dev, generator=gen) * 0.01 + 1e-3).half(),
+                               (torch.rand((Np, Kp // 128), device=dev, generator=gen) * -0.05).half(), Np, Kp)
+        W.build_tiled()
+        X = torch.randn((args.profile_prefill, Kp), device=dev, generator=gen).to(torch.bfloat16)
+        for _ in range(3):
+            Y = q4.gemm_prefill(W, X)
+        idx = [float(Y.abs().mean()), q4.prefill_kernel(Kp, args.profile_prefill)]
     elif args.profile_sampler:
         Y = torch.randn((B, N), device=dev, generator=gen) * 3
         noise = torch.zeros((B, 50), device=dev)
@@ -905,7 +917,8 @@ def run_profile_small(args) -> int:
         idx = [float(O.abs().mean())]
     torch.cuda.synchronize()
     q4.device_status()
-    case = "int8 head" if args.profile_head8 else "sampler" if args.profile_sampler else "attention"
+    case = ("int8 head" if args.profile_head8 else "sampler" if args.profile_sampler
+            else "prefill" if args.profile_prefill else "attention")
     print(json.dumps({"profile_case": case, "B": B, "idx": idx if isinstance(idx, list) else idx.cpu().tolist()}))
     return 0
 
@@ -925,10 +938,11 @@ def main():
     ap.add_argument("--profile-head8", action="store_true", help="run only a small int8-head case for ncu")
     ap.add_argument("--profile-sampler", action="store_true", help="run only a small sampler case for ncu")
     ap.add_argument("--profile-attn", action="store_true", help="run only a flash-decoding attention case for ncu")
+    ap.add_argument("--profile-prefill", type=int, default=0, help="run only a prefill GEMM case of this many tokens")
     args = ap.parse_args()
     if args.profile_step > 0:
         return run_profile_case(args)
-    if args.profile_head8 or args.profile_sampler or args.profile_attn:
+    if args.profile_head8 or args.profile_sampler or args.profile_attn or args.profile_prefill:
         return run_profile_small(args)
     if args.impl == "reference":
         return run_reference(args)
