@@ -717,7 +717,7 @@ def sampler_bench(q4, torch, dev, args):
         e1.record()
         torch.cuda.synchronize()
         out[f"b{B}_us_per_call"] = round(1e3 * e0.elapsed_time(e1) / (n * 20), 3)
-    out["kernel"] = "q4_sample_kernel (one 1024-thread CTA per row; k = 50, N = 65,536)"
+    out["kernel"] = "q4_sample_cluster_kernel (a cluster of 8 CTAs per row; k = 50, N = 65,536)"
     return out
 
 
