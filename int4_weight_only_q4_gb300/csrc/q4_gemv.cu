@@ -955,6 +955,30 @@ __global__ void __launch_bounds__(256) q4_xprep_kernel(const __grid_constant__ P
 // c - 1, whose values are already in registers.  The 64 scale/min bytes are written by lanes 0-3
 // and read by all lanes, which cp.async.wait_group + __syncwarp order.  Which warp takes which
 // tile changes no arithmetic.
+// Inclusive prefix sum of v over threads 0 .. kMaxMats-1 of the block (the other threads pass
+// anything; their results are meaningless), and the sum over those threads in *all.  Every thread
+// of the block calls it (it holds two block barriers); ws holds kMaxMats / 32 values.
+__device__ __forceinline__ int64_t scan_list(int64_t v, int64_t* ws, int64_t* all) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (w >= kMaxMats / 32) v = 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    if (w < kMaxMats / 32 && lane == 31) ws[w] = v;
+    __syncthreads();
+    int64_t base = 0, sum = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxMats / 32; ++j) {
+        base += j < w ? ws[j] : 0;
+        sum += ws[j];
+    }
+    *all = sum;
+    __syncthreads();  // ws is free for the next call
+    return base + v;
+}
+
 struct TileMat {
     const uint8_t* tiled;
     const uint4* xf;  // prepared activations, one 16-byte word per lane and fragment pair
@@ -983,56 +1007,60 @@ constexpr int kItemQ = 16;  // per-warp queue of tiles requested but not yet com
 template <int WARPS, int S, int BT, bool RO = false>
 __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __grid_constant__ TileParams p) {
     static_assert(S >= 2 && S < kItemQ, "ring depth");
+    static_assert(WARPS * 32 >= kMaxMats, "one thread per matrix in the prologue");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int prefix[kMaxMats + 1];   // this CTA's tiles in matrices [0, i)
     __shared__ int tfirst[kMaxMats];       // first tile of this CTA's row block in matrix i
     __shared__ int next_item;
     __shared__ int2 itemq[WARPS][kItemQ];  // (matrix, tile)
+    __shared__ int64_t scan_ws[kMaxMats / 32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int t = lane & 3, q = lane >> 2;
     const int B = p.B;
     unsigned char* ring = smem + static_cast<size_t>(warp) * S * kRecBytes;
-    if (threadIdx.x == 0) {
-        int acc = 0;
+    // This CTA's share of every matrix, thread i for matrix i (in parallel: a serial walk over a
+    // long list by one thread costs hundreds of cycles per matrix before any weight is requested),
+    // then prefix sums over the matrices by the first kMaxMats threads.
+    {
+        const int i = threadIdx.x;
+        const bool mine = i < p.n_mats;
+        const int T_all = mine ? (p.m[i].N + 15) >> 4 : 0;
+        const int Gi = mine ? p.m[i].K >> 7 : 1;
+        int first = 0, cnt = 0;
         if (p.contiguous) {
             // the list's tiles, matrix after matrix, as one run of records; CTA c takes the tiles
             // whose first record falls in [c R / grid, (c+1) R / grid)
-            int64_t R = 0;
-            for (int i = 0; i < p.n_mats; ++i) R += static_cast<int64_t>((p.m[i].N + 15) >> 4) * (p.m[i].K >> 7);
-            const int64_t nb = gridDim.x, c = blockIdx.x;
-            const int64_t lo = c * R / nb, hi = (c + 1) * R / nb;
-            int64_t cum = 0;
-            for (int i = 0; i < p.n_mats; ++i) {
-                const TileMat& m = p.m[i];
-                const int64_t T_all = (m.N + 15) >> 4, G = m.K >> 7;
+            const int64_t rec = static_cast<int64_t>(T_all) * Gi;
+            int64_t R;
+            const int64_t cum = scan_list(rec, scan_ws, &R) - rec;
+            if (mine) {
+                const int64_t nb = gridDim.x, c = blockIdx.x;
+                const int64_t lo = c * R / nb, hi = (c + 1) * R / nb;
                 // tiles t with cum + t G in [lo, hi)
-                int64_t t0 = lo > cum ? (lo - cum + G - 1) / G : 0;
-                int64_t t1 = hi > cum ? (hi - cum + G - 1) / G : 0;
+                int64_t t0 = lo > cum ? (lo - cum + Gi - 1) / Gi : 0;
+                int64_t t1 = hi > cum ? (hi - cum + Gi - 1) / Gi : 0;
                 t0 = t0 < T_all ? t0 : T_all;
                 t1 = t1 < T_all ? t1 : T_all;
-                prefix[i] = acc;
-                tfirst[i] = static_cast<int>(t0);
-                acc += static_cast<int>(t1 - t0);
-                cum += T_all * G;
+                first = static_cast<int>(t0);
+                cnt = static_cast<int>(t1 - t0);
             }
-        } else {
-            for (int i = 0; i < p.n_mats; ++i) {
-                const TileMat& m = p.m[i];
-                prefix[i] = acc;
-                tfirst[i] = 0;
-                if (static_cast<int>(blockIdx.x) < m.row_blocks) {
-                    const int T_all = (m.N + 15) >> 4;
-                    const int rb = (static_cast<int>(blockIdx.x) + m.rot) % m.row_blocks;
-                    const int t0 = static_cast<int>(static_cast<int64_t>(rb) * T_all / m.row_blocks);
-                    const int t1 = static_cast<int>(static_cast<int64_t>(rb + 1) * T_all / m.row_blocks);
-                    tfirst[i] = t0;
-                    acc += t1 - t0;
-                }
-            }
+        } else if (mine && static_cast<int>(blockIdx.x) < p.m[i].row_blocks) {
+            const TileMat& m = p.m[i];
+            const int rb = (static_cast<int>(blockIdx.x) + m.rot) % m.row_blocks;
+            first = static_cast<int>(static_cast<int64_t>(rb) * T_all / m.row_blocks);
+            cnt = static_cast<int>(static_cast<int64_t>(rb + 1) * T_all / m.row_blocks) - first;
         }
-        prefix[p.n_mats] = acc;
-        next_item = 0;
+        int64_t all;
+        const int incl = static_cast<int>(scan_list(static_cast<int64_t>(cnt), scan_ws, &all));
+        if (mine) {
+            prefix[i] = incl - cnt;
+            tfirst[i] = first;
+        }
+        if (i == 0) {
+            prefix[p.n_mats] = static_cast<int>(all);
+            next_item = 0;
+        }
     }
     __syncthreads();
     const int total = prefix[p.n_mats];
@@ -2792,8 +2820,19 @@ bool smem_attr_set(Fn fn, int dev) {
     const void* key = reinterpret_cast<const void*>(fn);
     for (int i = 0; i < n_done; ++i)
         if (done[i].fn == key && done[i].dev == dev) return true;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemLimit)) !=
-        cudaSuccess) {
+    // the raised limit plus the kernel's static shared memory must stay under the per-block maximum
+    cudaFuncAttributes fa{};
+    int optin = 0;
+    bool ok = cudaFuncGetAttributes(&fa, fn) == cudaSuccess &&
+              cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+              static_cast<size_t>(optin) > fa.sharedSizeBytes;
+    if (ok) {
+        size_t lim = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+        lim = lim < kSmemLimit ? lim : kSmemLimit;
+        ok = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(lim)) ==
+             cudaSuccess;
+    }
+    if (!ok) {
         (void)cudaGetLastError();  // not sticky: clear it so that later checks do not see it
         return false;
     }
