@@ -930,16 +930,127 @@ struct PrepParams {
     PrepJob j[kMaxMats];
 };
 
+// stage_x with LM for a whole matrix (g0 = 0, Gs = G), the same outputs bit for bit, with a
+// thread's pieces of x loaded U at a time before any is used: the pieces do not depend on one
+// another, so a thread waits for memory once per U pieces instead of once per piece.  The column
+// maxima are first reduced over the 16 lanes of a (group, column) and then taken by one shared
+// atomic.  When every piece fits in one round, the second pass reuses the registers.  Every thread
+// of the block calls this with nthr = blockDim.x (a multiple of 32).
+template <int BT, bool X8, int U>
+__device__ __forceinline__ void stage_x_batched(const uint16_t* x, int K, int B, int G, uint2* xs, float* ssum,
+                                                float* fac, unsigned* colmax, int tid, int nthr) {
+    const int items = G * B * 16;  // (group, column, chunk t, word i); (t, i) fastest
+    auto piece = [&](int idx) -> uint4 {
+        const int ti = idx & 15, gn = idx >> 4;
+        return *reinterpret_cast<const uint4*>(x + static_cast<size_t>(gn % B) * K + static_cast<size_t>(gn / B) * 128 +
+                                               (ti >> 2) * 32 + (ti & 3) * 8);
+    };
+    if (tid < 8) colmax[tid] = 0u;
+    __syncthreads();
+    uint4 v[U];
+    for (int r0 = 0; r0 < items; r0 += U * nthr) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = r0 + u * nthr + tid;
+            v[u] = idx < items ? piece(idx) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (r0 + u * nthr >= items) break;  // the same for every thread
+            const int idx = r0 + u * nthr + tid;
+            const uint32_t h[8] = {v[u].x << 16, v[u].x & 0xFFFF0000u, v[u].y << 16, v[u].y & 0xFFFF0000u,
+                                   v[u].z << 16, v[u].z & 0xFFFF0000u, v[u].w << 16, v[u].w & 0xFFFF0000u};
+            uint32_t mx = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx = max(mx, h[e] & 0x7FFFFFFFu);
+            float s = bf16lo_to_f32(v[u].x);
+            s += bf16hi_to_f32(v[u].x);
+            s += bf16lo_to_f32(v[u].y);
+            s += bf16hi_to_f32(v[u].y);
+            s += bf16lo_to_f32(v[u].z);
+            s += bf16hi_to_f32(v[u].z);
+            s += bf16lo_to_f32(v[u].w);
+            s += bf16hi_to_f32(v[u].w);
+            // the 16 lanes of one (group, column): items are whole multiples of 16, so these lanes
+            // are all in range or all out of it
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                s += __shfl_xor_sync(0xffffffffu, s, o);
+            }
+            if (idx < items && (idx & 15) == 0) {
+                const int gn = idx >> 4;
+                atomicMax(&colmax[gn % B], mx);
+                ssum[(gn / B) * 8 + gn % B] = s;
+            }
+        }
+    }
+    for (int idx = tid; idx < G * 8; idx += nthr)
+        if ((idx & 7) >= B) ssum[idx] = 0.f;
+    __syncthreads();
+    const bool one_round = items <= U * nthr;
+    for (int r0 = 0; r0 < items; r0 += U * nthr) {
+        if (!one_round) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int idx = r0 + u * nthr + tid;
+                v[u] = idx < items ? piece(idx) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = r0 + u * nthr + tid;
+            if (idx >= items) break;
+            const int ti = idx & 15, gn = idx >> 4;
+            const int n = gn % B, gl = gn / B;
+            const int tt = ti >> 2, i = ti & 3;
+            const int e = static_cast<int>(colmax[n] >> 23) - 127;  // colmax == 0: e = -127
+            int a = 120 - e;
+            a = a < 6 ? 6 : (a > 253 ? 253 : a);
+            // x * 2^a as two exact power-of-two products, so that 2^a itself need not be a float
+            const int a1 = a > 127 ? 127 : a;
+            const float m1 = __int_as_float((a1 + 127) << 23);
+            const float m2 = __int_as_float((a - a1 + 127) << 23);
+            uint2 p0, p1;
+            if constexpr (X8) {
+                p0.x = bf16x2_scale(__byte_perm(v[u].x, v[u].y, 0x5410), m1, m2);
+                p0.y = bf16x2_scale(__byte_perm(v[u].x, v[u].y, 0x7632), m1, m2);
+                p1.x = bf16x2_scale(__byte_perm(v[u].z, v[u].w, 0x5410), m1, m2);
+                p1.y = bf16x2_scale(__byte_perm(v[u].z, v[u].w, 0x7632), m1, m2);
+            } else {
+                p0.x = bf16x2_scale(__byte_perm(v[u].x, v[u].z, 0x5410), m1, m2);
+                p0.y = bf16x2_scale(__byte_perm(v[u].x, v[u].z, 0x7632), m1, m2 * 0.0625f);
+                p1.x = bf16x2_scale(__byte_perm(v[u].y, v[u].w, 0x5410), m1, m2);
+                p1.y = bf16x2_scale(__byte_perm(v[u].y, v[u].w, 0x7632), m1, m2 * 0.0625f);
+            }
+            const size_t li = (static_cast<size_t>(gl) * 4 + i) * 4 * BT + n * 4 + tt;
+            reinterpret_cast<uint4*>(xs)[li] = make_uint4(p0.x, p0.y, p1.x, p1.y);
+            if (ti == 0) {  // this thread wrote ssum[gl * 8 + n] in the first pass
+                const int es = a - 133, e1 = es < -63 ? -63 : es, e2 = es - e1;
+                ssum[gl * 8 + n] = (ssum[gl * 8 + n] * __int_as_float((e1 + 127) << 23)) *
+                                   __int_as_float((e2 + 127) << 23);
+            }
+        }
+    }
+    if (tid < 8) {
+        const int e = static_cast<int>(colmax[tid] >> 23) - 127;
+        int a = 120 - e;
+        a = a < 6 ? 6 : (a > 253 ? 253 : a);
+        fac[tid] = __int_as_float((133 - a + 127) << 23);  // 2^(133-a), 2^-120 .. 2^127
+    }
+}
+
+constexpr int kPrepThreads = 512;
+
 template <int BT, bool X8 = false>
-__global__ void __launch_bounds__(256) q4_xprep_kernel(const __grid_constant__ PrepParams p) {
+__global__ void __launch_bounds__(kPrepThreads) q4_xprep_kernel(const __grid_constant__ PrepParams p) {
     __shared__ unsigned colmax[8];
     // The tile kernel after this one may start at once: it streams weights (read-only) until its
     // own wait, which returns only when this grid is complete.
     allow_dependents();
     grid_dependency_wait();  // x may be the previous kernel's output
     const PrepJob& j = p.j[blockIdx.x];
-    stage_x<BT, true, SyncThreads, X8>(j.x, j.K, p.B, 0, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, 256,
-                                       SyncThreads{});
+    stage_x_batched<BT, X8, 16>(j.x, j.K, p.B, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, kPrepThreads);
 }
 
 // q4_tiles_ring_kernel: one CTA per SM, persistent over a list of independent matrices, no
@@ -2054,6 +2165,93 @@ __device__ __forceinline__ void st_cluster_u64(void* local, unsigned rank, unsig
     asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(ra), "l"(v) : "memory");
 }
 
+// q4_argmax_cluster_kernel: the q4_argmax_kernel result with each row split over a cluster of kAC
+// CTAs, so that every thread issues its few 16-byte loads at once (one memory round trip for a
+// 65,536-wide row instead of four).  CTA r of a row's cluster takes words [r n4 / kAC, (r+1) n4 / kAC)
+// of the row's 16-byte-aligned body (CTA 0 also the scalar head, the last CTA the scalar tail),
+// reduces them like q4_argmax_kernel and stores its best (value bits, index) into the shared memory
+// of CTA 0; after one cluster barrier CTA 0 merges the kAC candidates.  ranks_above is a total
+// order, so the split changes no result.
+constexpr int kAC = 8;  // CTAs per row: one portable-size cluster
+constexpr int kACThreads = 512;
+
+__global__ void __launch_bounds__(kACThreads) q4_argmax_cluster_kernel(const float* __restrict__ Y, int N,
+                                                                       int32_t* idx) {
+    __shared__ unsigned long long cand[kAC];  // CTA 0: every CTA's best
+    __shared__ float sv[kACThreads / 32];
+    __shared__ int si[kACThreads / 32];
+    grid_dependency_wait();  // the logits are usually the previous kernel's output
+    allow_dependents();
+    const int rank = static_cast<int>(blockIdx.x);  // the cluster spans the grid's x dimension (kAC)
+    const float* row = Y + static_cast<size_t>(blockIdx.y) * N;
+    float bv = -__int_as_float(0x7f800000);
+    int bi = 0x7fffffff;
+    auto consider = [&](float v, int i) {
+        if (ranks_above(v, i, bv, bi)) { bv = v; bi = i; }
+    };
+    const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(row) & 15u) >> 2);  // row is 4-byte aligned
+    const int head = min(N, (4 - mis) & 3);
+    const int n4 = (N - head) >> 2;
+    const int tail0 = head + 4 * n4;
+    const int tid = static_cast<int>(threadIdx.x);
+    if (rank == 0 && tid < head) consider(ld_dep_f32(row + tid), tid);
+    if (rank == kAC - 1 && tail0 + tid < N) consider(ld_dep_f32(row + tail0 + tid), tail0 + tid);
+    const int w0 = static_cast<int>(static_cast<int64_t>(n4) * rank / kAC);
+    const int w1 = static_cast<int>(static_cast<int64_t>(n4) * (rank + 1) / kAC);
+    const float4* row4 = reinterpret_cast<const float4*>(row + head);
+    constexpr int kU = 4;
+    for (int base = w0 + tid; base < w1; base += kU * kACThreads) {
+        float4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int j = base + u * kACThreads;
+            v[u] = j < w1 ? ld_dep_f4(row4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int j = base + u * kACThreads;
+            if (j < w1) {
+                const int i = head + 4 * j;
+                consider(v[u].x, i);
+                consider(v[u].y, i + 1);
+                consider(v[u].z, i + 2);
+                consider(v[u].w, i + 3);
+            }
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ranks_above(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    const int w = tid >> 5;
+    if ((tid & 31) == 0) { sv[w] = bv; si[w] = bi; }
+    __syncthreads();
+    if (w == 0) {
+        bv = tid < kACThreads / 32 ? sv[tid] : -__int_as_float(0x7f800000);
+        bi = tid < kACThreads / 32 ? si[tid] : 0x7fffffff;
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ranks_above(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        if (tid == 0)
+            st_cluster_u64(&cand[rank], 0u,
+                           (static_cast<unsigned long long>(__float_as_uint(bv)) << 32) | static_cast<uint32_t>(bi));
+    }
+    cluster_barrier();  // every thread of every CTA of the cluster reaches it
+    if (rank == 0 && tid == 0) {
+        bv = -__int_as_float(0x7f800000);
+        bi = 0x7fffffff;
+        for (int c = 0; c < kAC; ++c) {
+            const float v = __uint_as_float(static_cast<uint32_t>(cand[c] >> 32));
+            const int i = static_cast<int>(static_cast<uint32_t>(cand[c]));
+            if (ranks_above(v, i, bv, bi)) { bv = v; bi = i; }
+        }
+        idx[blockIdx.y] = bi == 0x7fffffff ? 0 : bi;
+    }
+}
+
 // VEC: 16-byte loads (row 16-byte aligned, N a multiple of 4); REG: the chunk's keys fit in
 // registers (kSCThreads * kSCRegs) and the row is read once
 template <bool VEC, bool REG>
@@ -2968,7 +3166,7 @@ q4_status tiles_prepare(const Knobs& k, const q4_matrix* mats, int n, const uint
                                 : bt == 4 ? q4_xprep_kernel<4, true> : q4_xprep_kernel<8, true>)
                              : (bt == 1 ? q4_xprep_kernel<1> : bt == 2 ? q4_xprep_kernel<2>
                                 : bt == 4 ? q4_xprep_kernel<4> : q4_xprep_kernel<8>);
-        const q4_status s = launch(pf, dev, static_cast<unsigned>(cnt), 256u, 0, stream, k.pdl, pp);
+        const q4_status s = launch(pf, dev, static_cast<unsigned>(cnt), static_cast<unsigned>(kPrepThreads), 0, stream, k.pdl, pp);
         if (s != Q4_OK) return s;
     }
     return Q4_OK;
@@ -3494,7 +3692,7 @@ extern "C" q4_status q4_gemm_prefill(const q4_matrix* W, const uint16_t* X, int6
             j.S = reinterpret_cast<float*>(w + G * 256 * 8);
             j.fac = j.S + G * 8;
         }
-        st = launch(q4_xprep_kernel<8>, dev, static_cast<unsigned>(pp.n), 256u, 0, cs, k.pdl, pp);
+        st = launch(q4_xprep_kernel<8>, dev, static_cast<unsigned>(pp.n), static_cast<unsigned>(kPrepThreads), 0, cs, k.pdl, pp);
         if (st != Q4_OK) return st;
         b0 = b1;
     }
@@ -3689,17 +3887,24 @@ extern "C" q4_status q4_argmax_f32(const float* Y, int B, int64_t N, int32_t* id
     if (!Y || !idx || B < 1 || B > kMaxB || N < 1 || N > 0x7fffffffLL) return Q4_ERR_INVALID_ARG;
     if (!aligned(Y, 4) || !aligned(idx, 4)) return Q4_ERR_MISALIGNED;
     if (fault_injected()) return Q4_ERR_CUDA;
+    const bool cl = env_int("Q4_ARGMAX_CLUSTER", 1) != 0;  // 0: one CTA per row (q4_argmax_kernel)
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(B));
-    cfg.blockDim = dim3(1024);
+    cfg.gridDim = cl ? dim3(kAC, static_cast<unsigned>(B)) : dim3(static_cast<unsigned>(B));
+    cfg.blockDim = dim3(cl ? kACThreads : 1024);
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = env_int("Q4_PDL", 1) != 0 ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kAC;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, q4_argmax_kernel, Y, static_cast<int>(N), idx) == cudaSuccess ? Q4_OK
-                                                                                                : Q4_ERR_CUDA;
+    cfg.numAttrs = cl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, cl ? q4_argmax_cluster_kernel : q4_argmax_kernel, Y, static_cast<int>(N), idx) ==
+                   cudaSuccess
+               ? Q4_OK
+               : Q4_ERR_CUDA;
 }
 
 extern "C" q4_status q4_argmax_key_f32(const float* Y, int B, int64_t N, int64_t index_base, int64_t* keys,

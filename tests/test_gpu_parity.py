@@ -318,7 +318,10 @@ def test_head_and_argmax_exact(q4, B):
             assert idx[b].item() == ref_idx[b]
 
 
-def test_argmax_ties_nan_and_layout(q4):
+@pytest.mark.parametrize("cluster", ["1", "0"])
+def test_argmax_ties_nan_and_layout(q4, monkeypatch, cluster):
+    """Both argmax kernels: a cluster of 8 CTAs per row (default) and one CTA per row."""
+    monkeypatch.setenv("Q4_ARGMAX_CLUSTER", cluster)
     y = np.random.default_rng(0).standard_normal((8, 70001)).astype(np.float32)
     y[0, 5] = y[0, 9] = 100.0               # tie: lowest index
     y[1, :] = 0.0; y[1, 3] = -0.0           # all equal: index 0
@@ -331,7 +334,7 @@ def test_argmax_ties_nan_and_layout(q4):
     assert got[0] == 5 and got[1] == 0 and got[2] == 123 and got[3] == 70000 and got[4] == 17
     # short and oddly aligned rows: scalar head, vector body and scalar tail of every size
     rng = np.random.default_rng(1)
-    for N in (1, 2, 3, 4, 5, 7, 9, 4097, 4099):
+    for N in (1, 2, 3, 4, 5, 7, 9, 31, 33, 4097, 4099, 65536, 65539):
         y = rng.standard_normal((8, N)).astype(np.float32)
         got = q4.argmax(torch.from_numpy(y).cuda()).cpu().numpy()
         assert got.tolist() == np.argmax(y, axis=1).tolist(), N
