@@ -940,9 +940,14 @@ template <int BT, bool X8, int U>
 __device__ __forceinline__ void stage_x_batched(const uint16_t* x, int K, int B, int G, uint2* xs, float* ssum,
                                                 float* fac, unsigned* colmax, int tid, int nthr) {
     const int items = G * B * 16;  // (group, column, chunk t, word i); (t, i) fastest
+    // gn / B as a multiply and shift: exact for gn < 2^16 (gn < G B <= 4096 here), and the product
+    // stays below 2^32 for gn < 2^13
+    const uint32_t binv = (1u << 19) / B + ((1u << 19) % B != 0 ? 1u : 0u);
+    auto div_b = [&](int gn) { return static_cast<int>((static_cast<uint32_t>(gn) * binv) >> 19); };
     auto piece = [&](int idx) -> uint4 {
         const int ti = idx & 15, gn = idx >> 4;
-        return *reinterpret_cast<const uint4*>(x + static_cast<size_t>(gn % B) * K + static_cast<size_t>(gn / B) * 128 +
+        const int gl = div_b(gn), n = gn - gl * B;
+        return *reinterpret_cast<const uint4*>(x + static_cast<size_t>(n) * K + static_cast<size_t>(gl) * 128 +
                                                (ti >> 2) * 32 + (ti & 3) * 8);
     };
     if (tid < 8) colmax[tid] = 0u;
@@ -980,8 +985,9 @@ __device__ __forceinline__ void stage_x_batched(const uint16_t* x, int K, int B,
             }
             if (idx < items && (idx & 15) == 0) {
                 const int gn = idx >> 4;
-                atomicMax(&colmax[gn % B], mx);
-                ssum[(gn / B) * 8 + gn % B] = s;
+                const int gl = div_b(gn), n = gn - gl * B;
+                atomicMax(&colmax[n], mx);
+                ssum[gl * 8 + n] = s;
             }
         }
     }
@@ -1002,7 +1008,7 @@ __device__ __forceinline__ void stage_x_batched(const uint16_t* x, int K, int B,
             const int idx = r0 + u * nthr + tid;
             if (idx >= items) break;
             const int ti = idx & 15, gn = idx >> 4;
-            const int n = gn % B, gl = gn / B;
+            const int gl = div_b(gn), n = gn - gl * B;
             const int tt = ti >> 2, i = ti & 3;
             const int e = static_cast<int>(colmax[n] >> 23) - 127;  // colmax == 0: e = -127
             int a = 120 - e;
@@ -1040,7 +1046,7 @@ __device__ __forceinline__ void stage_x_batched(const uint16_t* x, int K, int B,
     }
 }
 
-constexpr int kPrepThreads = 512;
+constexpr int kPrepThreads = 1024;
 
 template <int BT, bool X8 = false>
 __global__ void __launch_bounds__(kPrepThreads) q4_xprep_kernel(const __grid_constant__ PrepParams p) {
@@ -1050,7 +1056,7 @@ __global__ void __launch_bounds__(kPrepThreads) q4_xprep_kernel(const __grid_con
     allow_dependents();
     grid_dependency_wait();  // x may be the previous kernel's output
     const PrepJob& j = p.j[blockIdx.x];
-    stage_x_batched<BT, X8, 16>(j.x, j.K, p.B, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, kPrepThreads);
+    stage_x_batched<BT, X8, 8>(j.x, j.K, p.B, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, kPrepThreads);
 }
 
 // q4_tiles_ring_kernel: one CTA per SM, persistent over a list of independent matrices, no
