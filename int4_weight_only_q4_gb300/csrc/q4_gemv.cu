@@ -1461,8 +1461,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
         uint2* xs = reinterpret_cast<uint2*>(xsm);
         float* ssum = reinterpret_cast<float*>(xsm + static_cast<size_t>(G) * 256 * BT);
         float* fs = ssum + G * 8;
-        stage_x<BT, true, SyncThreads, Q8>(p.x, p.K, B, 0, G, xs, ssum, fs, colmax, static_cast<int>(threadIdx.x),
-                                           WARPS * 32, SyncThreads{});
+        stage_x_batched<BT, Q8, 2>(p.x, p.K, B, G, xs, ssum, fs, colmax, static_cast<int>(threadIdx.x), WARPS * 32);
         __syncthreads();
         xf = reinterpret_cast<const uint4*>(xs);
         Sb = ssum;
