@@ -331,16 +331,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) q4_prefill_tc_kernel(const __gr
     } else if (warp == 14) {
         // ---- scheduler: per group, the accumulator buffer is free, both half-groups' codes are in TMEM
         // and their activations have landed; then the MMA warp may issue the group
+        // The five waits of a step run side by side, one lane each (lane 0: the accumulator buffer;
+        // lanes 1-4: codes and activations of the two half-groups): a wait costs a few hundred cycles
+        // even on a completed phase, so five in sequence were most of a step's time.  The warp
+        // barrier after them orders every lane's acquire before the named barrier that releases
+        // the MMA warp.
         bool aborted = false;
         for (int g = 0; g < G; ++g) {
             if (!aborted) {  // after a wait gave up, the remaining steps go on garbage (the error word is set)
-                bool ok = tc_wait_warp(dempty + g % kDBufs, (static_cast<uint32_t>(g / kDBufs) & 1u) ^ 1u, abort_flag);
-                for (int hf = 0; hf < 2 && ok; ++hf) {
-                    const int h = 2 * g + hf;
-                    ok = tc_wait_warp(fullA + h % kAStages, static_cast<uint32_t>(h / kAStages) & 1u, abort_flag) &&
-                         tc_wait_warp(fullB + h % kBStages, static_cast<uint32_t>(h / kBStages) & 1u, abort_flag);
+                bool ok = true;
+                if (lane < 5) {
+                    uint64_t* bar;
+                    uint32_t parity;
+                    if (lane == 0) {
+                        bar = dempty + g % kDBufs;
+                        parity = (static_cast<uint32_t>(g / kDBufs) & 1u) ^ 1u;
+                    } else {
+                        const int h = 2 * g + ((lane - 1) >> 1);
+                        if (((lane - 1) & 1) == 0) {
+                            bar = fullA + h % kAStages;
+                            parity = static_cast<uint32_t>(h / kAStages) & 1u;
+                        } else {
+                            bar = fullB + h % kBStages;
+                            parity = static_cast<uint32_t>(h / kBStages) & 1u;
+                        }
+                    }
+                    ok = tc_wait(bar, parity, abort_flag);
                 }
-                aborted = !ok;
+                __syncwarp();
+                aborted = !__all_sync(0xffffffffu, ok);
             }
             asm volatile("bar.sync %0, 64;" ::"n"(kStepBar) : "memory");
         }
