@@ -298,128 +298,131 @@ __device__ __forceinline__ void group_epilogue(float (&acc)[4], const float (&c)
     acc[3] = fmaf(mb, S.y, acc[3]);
 }
 
-// A block-wide barrier as a callable (stage_x takes the barrier of its caller).
-struct SyncThreads {
-    __device__ void operator()() const { __syncthreads(); }
-};
-
-// Stage x[:, 128*g0 .. 128*(g0+Gs)) in B-fragment order, the per-group sums of x and the
-// per-column factors.  Column n gets a_n = 120 - e_n (e_n = exponent of the largest |x| of the
-// column's slice, a_n in [6, 253]): entries pairing with low nibbles hold x * 2^a_n, with high
-// nibbles x * 2^(a_n-4), and fac[n] = 2^(133 - a_n).  Exact for |x| < 2^121.
+// Stage x[:, 128*g0 .. 128*(g0+Gs)) for the mma B fragments, with the group sums of x and the
+// per-column factors: column n gets a_n = 120 - e_n (e_n = exponent of the largest |x| of the
+// column's slice, a_n in [6, 253]); entries pairing with low nibbles hold x * 2^a_n, with high
+// nibbles x * 2^(a_n-4), and fac[n] = 2^(133 - a_n).  Exact for |x| < 2^121.  S[gl][n] = sum over
+// the group (fixed order: 8 sequential adds, then a 16-lane xor tree).
 // Entry (gl, i, p, lane = 4n + t) (8 bytes) holds x[n][k], k = 128(g0+gl) + 32t + 8i + {2p, 2p+4,
-// 2p+1, 2p+5}; S[gl][n] = sum over the group (fixed order: 8 sequential adds, then a 16-lane xor
-// tree).  Every thread in [0, nthr) calls this; nthr is a multiple of 32.  colmax: 8 words of
-// scratch shared memory.
-// LM (for the prepared copy in global memory): entries (gl, i, 0) and (gl, i, 1) of lane L are one
-// 16-byte word, uint4 (gl * 4 + i) * 4BT + L, so that each of a warp's four loads per group is one
-// contiguous run; and the group sums are stored already divided by fac (S[gl][n] * 2^(a_n-133),
-// an exact power-of-two scaling), so that a consumer applies fac once per output instead of once
-// per group.
-// X8 (with LM, for the int8 head): the k pairing of the int8 operands instead -- word i of lane
-// (n, t) holds mma 2i and 2i+1, each as (x[k], x[k+2]) | (x[k+1], x[k+3]) with k = 32t + 4m for
-// mma m -- and no high-nibble factor.
-template <int BT, bool LM = false, typename Sync, bool X8 = false>
-__device__ __forceinline__ void stage_x(const uint16_t* x, int K, int B, int g0, int Gs, uint2* xs, float* ssum,
-                                        float* fac, unsigned* colmax, int tid, int nthr, Sync sync) {
-    const int items = Gs * B * 16;  // (local group, column, chunk t, word i); (t, i) fastest
-    const int iters = (items + nthr - 1) / nthr;
-    // a thread's first two 16-byte pieces of x are loaded once, both up front, and kept for the
-    // second pass (one round trip to memory instead of up to four); later pieces are read twice
-    uint4 vk[2];
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int idx = it * nthr + tid;
-        vk[it] = make_uint4(0u, 0u, 0u, 0u);
-        if (idx < items) {
-            const int ti = idx & 15, gn = idx >> 4;
-            vk[it] = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(gn % B) * K +
-                                                     static_cast<size_t>(g0 + gn / B) * 128 + (ti >> 2) * 32 +
-                                                     (ti & 3) * 8);
-        }
-    }
+// 2p+1, 2p+5}: in xfrag order (shared memory of the kernels that compute from it), or with LM
+// (prepared copies) entries (gl, i, 0) and (gl, i, 1) of lane L as one 16-byte word, uint4
+// (gl * 4 + i) * 4BT + L, so that each of a warp's four loads per group is one contiguous run,
+// and the group sums stored already divided by fac (S * 2^(a_n-133), an exact power-of-two
+// scaling).  X8 (with LM, for the int8 head): the k pairing of the int8 operands instead -- word
+// i of lane (n, t) holds mma 2i and 2i+1, each as (x[k], x[k+2]) | (x[k+1], x[k+3]) with
+// k = 32t + 4m for mma m -- and no high-nibble factor.
+// A thread's pieces of x are loaded U at a time before any is used (they do not depend on one
+// another, so a thread waits for memory once per U pieces); the column maxima are reduced over the
+// 16 lanes of a (group, column) before one shared atomic; when every piece fits in one round the
+// second pass reuses the registers.  Every thread in [0, nthr) calls this (nthr a multiple of 32);
+// sync is the callers' barrier over those threads; colmax: 8 words of scratch shared memory.
+template <int BT, bool LM, bool X8, int U, typename Sync>
+__device__ __forceinline__ void stage_x_batched(const uint16_t* x, int K, int B, int g0, int Gs, uint2* xs,
+                                                float* ssum, float* fac, unsigned* colmax, int tid, int nthr,
+                                                Sync sync) {
+    const int items = Gs * B * 16;  // (group, column, chunk t, word i); (t, i) fastest
+    // gn / B as a multiply and shift: exact for gn < 2^16 (gn < G B <= 4096 here), and the product
+    // stays below 2^32 for gn < 2^13
+    const uint32_t binv = (1u << 19) / B + ((1u << 19) % B != 0 ? 1u : 0u);
+    auto div_b = [&](int gn) { return static_cast<int>((static_cast<uint32_t>(gn) * binv) >> 19); };
+    auto piece = [&](int idx) -> uint4 {
+        const int ti = idx & 15, gn = idx >> 4;
+        const int gl = div_b(gn), n = gn - gl * B;
+        return *reinterpret_cast<const uint4*>(x + static_cast<size_t>(n) * K + static_cast<size_t>(g0 + gl) * 128 +
+                                               (ti >> 2) * 32 + (ti & 3) * 8);
+    };
     if (tid < 8) colmax[tid] = 0u;
     sync();
-    for (int it = 0; it < iters; ++it) {
-        const int idx = it * nthr + tid;
-        float s = 0.f;
-        const bool on = idx < items;
-        int gl = 0, n = 0;
-        if (on) {
-            const int ti = idx & 15;
-            const int gn = idx >> 4;
-            n = gn % B;
-            gl = gn / B;
-            const int tt = ti >> 2, i = ti & 3;
-            const uint4 v = it == 0 ? vk[0] : it == 1 ? vk[1] : *reinterpret_cast<const uint4*>(
-                x + static_cast<size_t>(n) * K + static_cast<size_t>(g0 + gl) * 128 + tt * 32 + i * 8);
+    uint4 v[U];
+    for (int r0 = 0; r0 < items; r0 += U * nthr) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = r0 + u * nthr + tid;
+            v[u] = idx < items ? piece(idx) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (r0 + u * nthr >= items) break;  // the same for every thread
+            const int idx = r0 + u * nthr + tid;
+            const uint32_t h[8] = {v[u].x << 16, v[u].x & 0xFFFF0000u, v[u].y << 16, v[u].y & 0xFFFF0000u,
+                                   v[u].z << 16, v[u].z & 0xFFFF0000u, v[u].w << 16, v[u].w & 0xFFFF0000u};
             uint32_t mx = 0;
-            const uint32_t h[8] = {v.x << 16, v.x & 0xFFFF0000u, v.y << 16, v.y & 0xFFFF0000u,
-                                   v.z << 16, v.z & 0xFFFF0000u, v.w << 16, v.w & 0xFFFF0000u};
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx = max(mx, h[e] & 0x7FFFFFFFu);
-            atomicMax(&colmax[n], mx);
-            s = bf16lo_to_f32(v.x);
-            s += bf16hi_to_f32(v.x);
-            s += bf16lo_to_f32(v.y);
-            s += bf16hi_to_f32(v.y);
-            s += bf16lo_to_f32(v.z);
-            s += bf16hi_to_f32(v.z);
-            s += bf16lo_to_f32(v.w);
-            s += bf16hi_to_f32(v.w);
+            float s = bf16lo_to_f32(v[u].x);
+            s += bf16hi_to_f32(v[u].x);
+            s += bf16lo_to_f32(v[u].y);
+            s += bf16hi_to_f32(v[u].y);
+            s += bf16lo_to_f32(v[u].z);
+            s += bf16hi_to_f32(v[u].z);
+            s += bf16lo_to_f32(v[u].w);
+            s += bf16hi_to_f32(v[u].w);
+            // the 16 lanes of one (group, column): items are whole multiples of 16, so these lanes
+            // are all in range or all out of it
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                s += __shfl_xor_sync(0xffffffffu, s, o);
+            }
+            if (idx < items && (idx & 15) == 0) {
+                const int gn = idx >> 4;
+                const int gl = div_b(gn), n = gn - gl * B;
+                atomicMax(&colmax[n], mx);
+                ssum[gl * 8 + n] = s;
+            }
         }
-        s += __shfl_xor_sync(0xffffffffu, s, 8);
-        s += __shfl_xor_sync(0xffffffffu, s, 4);
-        s += __shfl_xor_sync(0xffffffffu, s, 2);
-        s += __shfl_xor_sync(0xffffffffu, s, 1);
-        if (on && (idx & 15) == 0) ssum[gl * 8 + n] = s;
     }
     for (int idx = tid; idx < Gs * 8; idx += nthr)
         if ((idx & 7) >= B) ssum[idx] = 0.f;
     sync();
-    for (int it = 0, idx = tid; idx < items; ++it, idx += nthr) {
-        const int ti = idx & 15;
-        const int gn = idx >> 4;
-        const int n = gn % B;
-        const int gl = gn / B;
-        const int tt = ti >> 2, i = ti & 3;
-        const int e = static_cast<int>(colmax[n] >> 23) - 127;  // colmax == 0: e = -127
-        int a = 120 - e;
-        a = a < 6 ? 6 : (a > 253 ? 253 : a);
-        const uint4 v = it == 0 ? vk[0] : it == 1 ? vk[1] : *reinterpret_cast<const uint4*>(
-            x + static_cast<size_t>(n) * K + static_cast<size_t>(g0 + gl) * 128 + tt * 32 + i * 8);
-        // x * 2^a as two exact power-of-two products, so that 2^a itself need not be a float
-        const int a1 = a > 127 ? 127 : a;
-        const float m1 = __int_as_float((a1 + 127) << 23);
-        const float m2 = __int_as_float((a - a1 + 127) << 23);
-        uint2 p0, p1;
-        if constexpr (X8) {
-            p0.x = bf16x2_scale(__byte_perm(v.x, v.y, 0x5410), m1, m2);
-            p0.y = bf16x2_scale(__byte_perm(v.x, v.y, 0x7632), m1, m2);
-            p1.x = bf16x2_scale(__byte_perm(v.z, v.w, 0x5410), m1, m2);
-            p1.y = bf16x2_scale(__byte_perm(v.z, v.w, 0x7632), m1, m2);
-        } else {
-            p0.x = __byte_perm(v.x, v.z, 0x5410);
-            p0.y = __byte_perm(v.x, v.z, 0x7632);
-            p1.x = __byte_perm(v.y, v.w, 0x5410);
-            p1.y = __byte_perm(v.y, v.w, 0x7632);
-            p0.x = bf16x2_scale(p0.x, m1, m2);
-            p1.x = bf16x2_scale(p1.x, m1, m2);
-            p0.y = bf16x2_scale(p0.y, m1, m2 * 0.0625f);
-            p1.y = bf16x2_scale(p1.y, m1, m2 * 0.0625f);
-        }
-        if constexpr (LM) {
-            const size_t li = (static_cast<size_t>(gl) * 4 + i) * 4 * BT + n * 4 + tt;
-            reinterpret_cast<uint4*>(xs)[li] = make_uint4(p0.x, p0.y, p1.x, p1.y);
-            if (ti == 0) {  // this thread wrote ssum[gl * 8 + n] in the first pass
-                const int e = a - 133, e1 = e < -63 ? -63 : e, e2 = e - e1;
-                ssum[gl * 8 + n] = (ssum[gl * 8 + n] * __int_as_float((e1 + 127) << 23)) *
-                                   __int_as_float((e2 + 127) << 23);
+    const bool one_round = items <= U * nthr;
+    for (int r0 = 0; r0 < items; r0 += U * nthr) {
+        if (!one_round) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int idx = r0 + u * nthr + tid;
+                v[u] = idx < items ? piece(idx) : make_uint4(0u, 0u, 0u, 0u);
             }
-        } else {
-            const size_t base = xfrag_index<BT>(gl, i, 0) + n * 4 + tt;
-            xs[base] = p0;
-            xs[base + 4 * BT] = p1;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = r0 + u * nthr + tid;
+            if (idx >= items) break;
+            const int ti = idx & 15, gn = idx >> 4;
+            const int gl = div_b(gn), n = gn - gl * B;
+            const int tt = ti >> 2, i = ti & 3;
+            const int e = static_cast<int>(colmax[n] >> 23) - 127;  // colmax == 0: e = -127
+            int a = 120 - e;
+            a = a < 6 ? 6 : (a > 253 ? 253 : a);
+            // x * 2^a as two exact power-of-two products, so that 2^a itself need not be a float
+            const int a1 = a > 127 ? 127 : a;
+            const float m1 = __int_as_float((a1 + 127) << 23);
+            const float m2 = __int_as_float((a - a1 + 127) << 23);
+            uint2 p0, p1;
+            if constexpr (X8) {
+                p0.x = bf16x2_scale(__byte_perm(v[u].x, v[u].y, 0x5410), m1, m2);
+                p0.y = bf16x2_scale(__byte_perm(v[u].x, v[u].y, 0x7632), m1, m2);
+                p1.x = bf16x2_scale(__byte_perm(v[u].z, v[u].w, 0x5410), m1, m2);
+                p1.y = bf16x2_scale(__byte_perm(v[u].z, v[u].w, 0x7632), m1, m2);
+            } else {
+                p0.x = bf16x2_scale(__byte_perm(v[u].x, v[u].z, 0x5410), m1, m2);
+                p0.y = bf16x2_scale(__byte_perm(v[u].x, v[u].z, 0x7632), m1, m2 * 0.0625f);
+                p1.x = bf16x2_scale(__byte_perm(v[u].y, v[u].w, 0x5410), m1, m2);
+                p1.y = bf16x2_scale(__byte_perm(v[u].y, v[u].w, 0x7632), m1, m2 * 0.0625f);
+            }
+            if constexpr (LM) {
+                const size_t li = (static_cast<size_t>(gl) * 4 + i) * 4 * BT + n * 4 + tt;
+                reinterpret_cast<uint4*>(xs)[li] = make_uint4(p0.x, p0.y, p1.x, p1.y);
+                if (ti == 0) {  // this thread wrote ssum[gl * 8 + n] in the first pass
+                    const int es = a - 133, e1 = es < -63 ? -63 : es, e2 = es - e1;
+                    ssum[gl * 8 + n] = (ssum[gl * 8 + n] * __int_as_float((e1 + 127) << 23)) *
+                                       __int_as_float((e2 + 127) << 23);
+                }
+            } else {
+                const size_t base = xfrag_index<BT>(gl, i, 0) + n * 4 + tt;
+                xs[base] = p0;
+                xs[base + 4 * BT] = p1;
+            }
         }
     }
     if (tid < 8) {
@@ -710,7 +713,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_direct_kernel(const __grid_c
         float* fac = ssum + cs.Gs * 8;
         unsigned* colmax = reinterpret_cast<unsigned*>(fac + 8);
         float* part = reinterpret_cast<float*>(colmax + 8);
-        stage_x<BT>(m.x, m.K, B, cs.g0, cs.Gs, xs, ssum, fac, colmax, tid, NT, [] { __syncthreads(); });
+        stage_x_batched<BT, false, false, 1>(m.x, m.K, B, cs.g0, cs.Gs, xs, ssum, fac, colmax, tid, NT,
+                                             [] { __syncthreads(); });
         __syncthreads();
         const float f0 = fac[2 * t], f1 = fac[2 * t + 1];
 
@@ -859,7 +863,8 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) q4_stream_kernel(const __grid
         float* fac = ssum + s.Gs * 8;
         unsigned* colmax = reinterpret_cast<unsigned*>(fac + 8);
         float* part = reinterpret_cast<float*>(colmax + 8);
-        stage_x<BT>(m.x, m.K, B, s.g0, s.Gs, xs, ssum, fac, colmax, tid, NT, [] { consumer_sync<NT>(); });
+        stage_x_batched<BT, false, false, 1>(m.x, m.K, B, s.g0, s.Gs, xs, ssum, fac, colmax, tid, NT,
+                                             [] { consumer_sync<NT>(); });
         consumer_sync<NT>();
         const float f0 = fac[2 * t], f1 = fac[2 * t + 1];
         for (int pass = 0, t0 = 0; t0 < s.T; ++pass, t0 += m.tiles_per_pass) {
@@ -912,7 +917,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) q4_stream_kernel(const __grid
 }
 
 // ================================================================== activation prep + tile kernel
-// q4_xprep_kernel: one CTA per matrix stages its activations once, in global memory, as stage_x
+// q4_xprep_kernel: one CTA per matrix stages its activations once, in global memory, as stage_x_batched
 // does in shared memory for the kernels above (layout LM): x in B-fragment order scaled per
 // column, the per-group sums of x divided by the column factors, and the column factors.
 struct PrepJob {
@@ -930,122 +935,6 @@ struct PrepParams {
     PrepJob j[kMaxMats];
 };
 
-// stage_x with LM for a whole matrix (g0 = 0, Gs = G), the same outputs bit for bit, with a
-// thread's pieces of x loaded U at a time before any is used: the pieces do not depend on one
-// another, so a thread waits for memory once per U pieces instead of once per piece.  The column
-// maxima are first reduced over the 16 lanes of a (group, column) and then taken by one shared
-// atomic.  When every piece fits in one round, the second pass reuses the registers.  Every thread
-// of the block calls this with nthr = blockDim.x (a multiple of 32).
-template <int BT, bool X8, int U>
-__device__ __forceinline__ void stage_x_batched(const uint16_t* x, int K, int B, int G, uint2* xs, float* ssum,
-                                                float* fac, unsigned* colmax, int tid, int nthr) {
-    const int items = G * B * 16;  // (group, column, chunk t, word i); (t, i) fastest
-    // gn / B as a multiply and shift: exact for gn < 2^16 (gn < G B <= 4096 here), and the product
-    // stays below 2^32 for gn < 2^13
-    const uint32_t binv = (1u << 19) / B + ((1u << 19) % B != 0 ? 1u : 0u);
-    auto div_b = [&](int gn) { return static_cast<int>((static_cast<uint32_t>(gn) * binv) >> 19); };
-    auto piece = [&](int idx) -> uint4 {
-        const int ti = idx & 15, gn = idx >> 4;
-        const int gl = div_b(gn), n = gn - gl * B;
-        return *reinterpret_cast<const uint4*>(x + static_cast<size_t>(n) * K + static_cast<size_t>(gl) * 128 +
-                                               (ti >> 2) * 32 + (ti & 3) * 8);
-    };
-    if (tid < 8) colmax[tid] = 0u;
-    __syncthreads();
-    uint4 v[U];
-    for (int r0 = 0; r0 < items; r0 += U * nthr) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int idx = r0 + u * nthr + tid;
-            v[u] = idx < items ? piece(idx) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (r0 + u * nthr >= items) break;  // the same for every thread
-            const int idx = r0 + u * nthr + tid;
-            const uint32_t h[8] = {v[u].x << 16, v[u].x & 0xFFFF0000u, v[u].y << 16, v[u].y & 0xFFFF0000u,
-                                   v[u].z << 16, v[u].z & 0xFFFF0000u, v[u].w << 16, v[u].w & 0xFFFF0000u};
-            uint32_t mx = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mx = max(mx, h[e] & 0x7FFFFFFFu);
-            float s = bf16lo_to_f32(v[u].x);
-            s += bf16hi_to_f32(v[u].x);
-            s += bf16lo_to_f32(v[u].y);
-            s += bf16hi_to_f32(v[u].y);
-            s += bf16lo_to_f32(v[u].z);
-            s += bf16hi_to_f32(v[u].z);
-            s += bf16lo_to_f32(v[u].w);
-            s += bf16hi_to_f32(v[u].w);
-            // the 16 lanes of one (group, column): items are whole multiples of 16, so these lanes
-            // are all in range or all out of it
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
-                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                s += __shfl_xor_sync(0xffffffffu, s, o);
-            }
-            if (idx < items && (idx & 15) == 0) {
-                const int gn = idx >> 4;
-                const int gl = div_b(gn), n = gn - gl * B;
-                atomicMax(&colmax[n], mx);
-                ssum[gl * 8 + n] = s;
-            }
-        }
-    }
-    for (int idx = tid; idx < G * 8; idx += nthr)
-        if ((idx & 7) >= B) ssum[idx] = 0.f;
-    __syncthreads();
-    const bool one_round = items <= U * nthr;
-    for (int r0 = 0; r0 < items; r0 += U * nthr) {
-        if (!one_round) {
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int idx = r0 + u * nthr + tid;
-                v[u] = idx < items ? piece(idx) : make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int idx = r0 + u * nthr + tid;
-            if (idx >= items) break;
-            const int ti = idx & 15, gn = idx >> 4;
-            const int gl = div_b(gn), n = gn - gl * B;
-            const int tt = ti >> 2, i = ti & 3;
-            const int e = static_cast<int>(colmax[n] >> 23) - 127;  // colmax == 0: e = -127
-            int a = 120 - e;
-            a = a < 6 ? 6 : (a > 253 ? 253 : a);
-            // x * 2^a as two exact power-of-two products, so that 2^a itself need not be a float
-            const int a1 = a > 127 ? 127 : a;
-            const float m1 = __int_as_float((a1 + 127) << 23);
-            const float m2 = __int_as_float((a - a1 + 127) << 23);
-            uint2 p0, p1;
-            if constexpr (X8) {
-                p0.x = bf16x2_scale(__byte_perm(v[u].x, v[u].y, 0x5410), m1, m2);
-                p0.y = bf16x2_scale(__byte_perm(v[u].x, v[u].y, 0x7632), m1, m2);
-                p1.x = bf16x2_scale(__byte_perm(v[u].z, v[u].w, 0x5410), m1, m2);
-                p1.y = bf16x2_scale(__byte_perm(v[u].z, v[u].w, 0x7632), m1, m2);
-            } else {
-                p0.x = bf16x2_scale(__byte_perm(v[u].x, v[u].z, 0x5410), m1, m2);
-                p0.y = bf16x2_scale(__byte_perm(v[u].x, v[u].z, 0x7632), m1, m2 * 0.0625f);
-                p1.x = bf16x2_scale(__byte_perm(v[u].y, v[u].w, 0x5410), m1, m2);
-                p1.y = bf16x2_scale(__byte_perm(v[u].y, v[u].w, 0x7632), m1, m2 * 0.0625f);
-            }
-            const size_t li = (static_cast<size_t>(gl) * 4 + i) * 4 * BT + n * 4 + tt;
-            reinterpret_cast<uint4*>(xs)[li] = make_uint4(p0.x, p0.y, p1.x, p1.y);
-            if (ti == 0) {  // this thread wrote ssum[gl * 8 + n] in the first pass
-                const int es = a - 133, e1 = es < -63 ? -63 : es, e2 = es - e1;
-                ssum[gl * 8 + n] = (ssum[gl * 8 + n] * __int_as_float((e1 + 127) << 23)) *
-                                   __int_as_float((e2 + 127) << 23);
-            }
-        }
-    }
-    if (tid < 8) {
-        const int e = static_cast<int>(colmax[tid] >> 23) - 127;
-        int a = 120 - e;
-        a = a < 6 ? 6 : (a > 253 ? 253 : a);
-        fac[tid] = __int_as_float((133 - a + 127) << 23);  // 2^(133-a), 2^-120 .. 2^127
-    }
-}
-
 constexpr int kPrepThreads = 1024;
 
 template <int BT, bool X8 = false>
@@ -1056,7 +945,8 @@ __global__ void __launch_bounds__(kPrepThreads) q4_xprep_kernel(const __grid_con
     allow_dependents();
     grid_dependency_wait();  // x may be the previous kernel's output
     const PrepJob& j = p.j[blockIdx.x];
-    stage_x_batched<BT, X8, 8>(j.x, j.K, p.B, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x, kPrepThreads);
+    stage_x_batched<BT, true, X8, 8>(j.x, j.K, p.B, 0, j.K >> 7, j.xf, j.S, j.fac, colmax, threadIdx.x,
+                                     kPrepThreads, [] { __syncthreads(); });
 }
 
 // q4_tiles_ring_kernel: one CTA per SM, persistent over a list of independent matrices, no
@@ -1326,7 +1216,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
 // shared memory (slot 0 for the first, slot 1 for the last) and count themselves in the ticket of
 // the tile's first warp; the warp that completes the count adds the partials in warp (= record)
 // order and writes Y.  Nothing is shared between CTAs and nothing outlives the launch.
-// XS: the CTA stages the activations itself (stage_x, layout LM) into shared memory after its
+// XS: the CTA stages the activations itself (stage_x_batched, layout LM) into shared memory after its
 // grid-dependency wait, while its first weight records are already on the way; otherwise they
 // come prepared from q4_xprep_kernel in global memory.
 // The split depends on N, K and the SM count only, so each batch column is computed in the same
@@ -1461,7 +1351,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
         uint2* xs = reinterpret_cast<uint2*>(xsm);
         float* ssum = reinterpret_cast<float*>(xsm + static_cast<size_t>(G) * 256 * BT);
         float* fs = ssum + G * 8;
-        stage_x_batched<BT, Q8, 2>(p.x, p.K, B, G, xs, ssum, fs, colmax, static_cast<int>(threadIdx.x), WARPS * 32);
+        stage_x_batched<BT, true, Q8, 2>(p.x, p.K, B, 0, G, xs, ssum, fs, colmax, static_cast<int>(threadIdx.x),
+                                         WARPS * 32, [] { __syncthreads(); });
         __syncthreads();
         xf = reinterpret_cast<const uint4*>(xs);
         Sb = ssum;
