@@ -140,6 +140,20 @@ __device__ __forceinline__ uint4 lds128(const unsigned char* p) {
     return r;
 }
 
+__device__ __forceinline__ uint4 lds128_s(uint32_t a) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+    return r;
+}
+__device__ __forceinline__ uint2 lds64_s(uint32_t a) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
+    return r;
+}
+__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ uint2 lds64(const unsigned char* p) {
     uint2 r;
     asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(smem_addr(p)));
@@ -1026,6 +1040,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
     const int t = lane & 3, q = lane >> 2;
     const int B = p.B;
     unsigned char* ring = smem + static_cast<size_t>(warp) * S * kRecBytes;
+    const uint32_t ring_s = smem_addr(ring) + 16u * static_cast<uint32_t>(lane);  // this lane's bytes of slot 0
     // This CTA's share of every matrix, thread i for matrix i (in parallel: a serial walk over a
     // long list by one thread costs hundreds of cycles per matrix before any weight is requested),
     // then prefix sums over the matrices by the first kMaxMats threads.
@@ -1098,10 +1113,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
             }
         }
         if (ld_left > 0) {
-            unsigned char* dst = ring + slot_off + 16 * lane;
-            cp_async16(dst, ld_ptr);
-            cp_async16(dst + 512, ld_ptr + 512);
-            if (lane < 4) cp_async16(dst + 1024, ld_ptr + 1024);
+            const uint32_t dst = ring_s + static_cast<uint32_t>(slot_off);
+            cp_async16_s(dst, ld_ptr);
+            cp_async16_s(dst + 512, ld_ptr + 512);
+            if (lane < 4) cp_async16_s(dst + 1024, ld_ptr + 1024);
             ld_ptr += kRecBytes;
             --ld_left;
         }
@@ -1140,14 +1155,16 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_tiles_ring_kernel(const __gr
     auto step = [&]() -> bool {
         cp_async_wait<S - 2>();  // this step's record has landed
         __syncwarp();
+        // plain coherent loads: the prepared activations were written by the kernel before, and the
+        // grid-dependency wait above them is a compiler barrier for memory accesses
         uint4 xv[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) xv[j] = ld_dep_u4(xg + j * (4 * BT));
-        const uint2 sv = ld_dep_u2(Sg);
-        const unsigned char* rec = ring + rd;
-        const uint4 qa = lds128(rec + 16 * lane);
-        const uint4 qb = lds128(rec + 512 + 16 * lane);
-        const uint2 sc = lds64(rec + 1024 + 8 * q);
+        for (int j = 0; j < 4; ++j) xv[j] = xg[j * (4 * BT)];
+        const uint2 sv = *reinterpret_cast<const uint2*>(Sg);
+        const uint32_t rec = ring_s + static_cast<uint32_t>(rd);
+        const uint4 qa = lds128_s(rec);
+        const uint4 qb = lds128_s(rec + 512);
+        const uint2 sc = lds64_s(rec - 16u * static_cast<uint32_t>(lane) + 1024u + 8u * static_cast<uint32_t>(q));
         issue(prev);  // S - 1 records ahead, into the slot read one step ago
         prev = rd;
         rd = rd + kRecBytes == S * kRecBytes ? 0 : rd + kRecBytes;
