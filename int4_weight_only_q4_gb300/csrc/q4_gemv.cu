@@ -1335,20 +1335,21 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
     const uint8_t* ld_ptr = p.tiled + (static_cast<size_t>(t0) * G + r0) * kRec + lane_off;
     int ld_left = n;
     if (lane == 0 && n > 0 && pf > 0) prefetch_l2_bulk(ld_ptr, static_cast<uint32_t>(min(n, pf) * kRec));
+    const uint32_t ring_s = smem_addr(ring) + static_cast<uint32_t>(lane_off);  // this lane's bytes of slot 0
     auto issue = [&](int slot_off) {
         if (ld_left > 0) {
             if (lane == 0 && pf > 0 && ld_left > pf)
                 prefetch_l2_bulk(ld_ptr + static_cast<size_t>(pf) * kRec, kRec);
-            unsigned char* dst = ring + slot_off + lane_off;
+            const uint32_t dst = ring_s + static_cast<uint32_t>(slot_off);
             if constexpr (Q8) {
-                cp_async16(dst, ld_ptr);
-                cp_async16(dst + 16, ld_ptr + 16);
-                cp_async16(dst + 1024, ld_ptr + 1024);
-                cp_async16(dst + 1040, ld_ptr + 1040);
+                cp_async16_s(dst, ld_ptr);
+                cp_async16_s(dst + 16, ld_ptr + 16);
+                cp_async16_s(dst + 1024, ld_ptr + 1024);
+                cp_async16_s(dst + 1040, ld_ptr + 1040);
             } else {
-                cp_async16(dst, ld_ptr);
-                cp_async16(dst + 512, ld_ptr + 512);
-                if (lane < 4) cp_async16(dst + 1024, ld_ptr + 1024);
+                cp_async16_s(dst, ld_ptr);
+                cp_async16_s(dst + 512, ld_ptr + 512);
+                if (lane < 4) cp_async16_s(dst + 1024, ld_ptr + 1024);
             }
             ld_ptr += kRec;
             --ld_left;
@@ -1380,13 +1381,15 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
         Sb = p.S;
         fac = p.fac;
     }
-    auto ldx4 = [&](const uint4* a) -> uint4 {  // XS: explicit shared-memory loads
+    // XS: explicit shared-memory loads; else plain coherent loads of the prepared copy (written by
+    // the kernel before: the grid-dependency wait above is a compiler barrier for memory accesses)
+    auto ldx4 = [&](const uint4* a) -> uint4 {
         if constexpr (XS) return lds128(reinterpret_cast<const unsigned char*>(a));
-        else return ld_dep_u4(a);
+        else return *a;
     };
     auto ldx2 = [&](const float* a) -> uint2 {
         if constexpr (XS) return lds64(reinterpret_cast<const unsigned char*>(a));
-        else return ld_dep_u2(a);
+        else return *reinterpret_cast<const uint2*>(a);
     };
     auto ldf = [&](const float* a) -> float {
         if constexpr (XS) return *a;
@@ -1480,11 +1483,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
         uint4 xv[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) xv[j] = ldx4(xg + j * (4 * BT));
-        const unsigned char* rec = ring + rd;
+        const uint32_t rec = ring_s + static_cast<uint32_t>(rd);  // this lane's bytes of the record
         if constexpr (Q8) {
             const uint2 sv = ldx2(Sg);
-            const uint4 ra0 = lds128(rec + 32 * lane), ra1 = lds128(rec + 32 * lane + 16);
-            const uint4 rb0 = lds128(rec + 1024 + 32 * lane), rb1 = lds128(rec + 1024 + 32 * lane + 16);
+            const uint4 ra0 = lds128_s(rec), ra1 = lds128_s(rec + 16);
+            const uint4 rb0 = lds128_s(rec + 1024), rb1 = lds128_s(rec + 1040);
             issue(prev);  // S - 1 records ahead, into the slot read one step ago
             prev = rd;
             rd = rd + kRec == S * kRec ? 0 : rd + kRec;
@@ -1498,9 +1501,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) q4_flat_kernel(const __grid_con
             Sg += 8;
         } else {
             const uint2 sv = ldx2(Sg);
-            const uint4 qa = lds128(rec + 16 * lane);
-            const uint4 qb = lds128(rec + 512 + 16 * lane);
-            const uint2 sc = lds64(rec + 1024 + 8 * q);
+            const uint4 qa = lds128_s(rec);
+            const uint4 qb = lds128_s(rec + 512);
+            const uint2 sc = lds64_s(rec - static_cast<uint32_t>(lane_off) + 1024u + 8u * static_cast<uint32_t>(q));
             issue(prev);  // S - 1 records ahead, into the slot read one step ago
             prev = rd;
             rd = rd + kRec == S * kRec ? 0 : rd + kRec;
