@@ -772,7 +772,8 @@ def attention_bench(q4, torch, dev, args):
     algorithmic bytes (keys, values, queries, outputs)."""
     Hq, Hkv, D = 24, 6, 128
     peak, src = measured_peak_gbs()
-    out = {"heads": f"{Hq} query / {Hkv} KV heads, head_dim {D}", "chunks_per_kv_head": int(q4.lib.q4_flash_decode_chunks(Hkv, 0))}
+    out = {"heads": f"{Hq} query / {Hkv} KV heads, head_dim {D}", "chunk_capacity_per_kv_head": int(q4.lib.q4_flash_decode_chunks(Hkv, 0)),
+           "chunks_in_use": "at most ceil(max_len / 32) per KV head (63 for the page's 2,000 positions)"}
     for name, B, L, layers, C in (("page_b1_2000", 1, 2000, 36, 0), ("page_b1_2000_16chunks", 1, 2000, 36, 16),
                                   ("long_b8_8192", 8, 8192, 2, 0)):
         g = torch.Generator(device=dev).manual_seed(args.seed)

@@ -446,7 +446,8 @@ q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float* Y, int32_
  *   B, n_kv_heads 1..65535;  1 <= max_len <= 2^30;  scale finite.
  *   n_chunks chunks per KV head at most, 1..4096, or 0 for the default of
  *            about eight per SM for one sequence (q4_flash_decode_chunks
- *            reports it).  The chunk length is ceil(len_b / chunks) rounded up
+ *            reports it), but no more than ceil(max_len / 32) (a shorter cache
+ *            has no more chunks than that).  The chunk length is ceil(len_b / chunks) rounded up
  *            to 16 and at least 32 positions, so a sequence's result does not
  *            depend on B or on the other sequences.
  *   O        device fp32 [B, n_q_heads, head_dim], 4-byte aligned.
@@ -460,9 +461,10 @@ q4_status q8_head(const q8_matrix* W, const uint16_t* X, int B, float* Y, int32_
  * group, chunks, max_len or scale; Q4_ERR_UNSUPPORTED_SHAPE for another
  * head_dim; Q4_ERR_MISALIGNED; Q4_ERR_WORKSPACE if ws_bytes is too small.
  */
-/* Chunks per KV head that q4_flash_decode uses for this request (n_chunks itself
- * when > 0; the default needs the current device's SM count); 0 for invalid
- * arguments or when the device cannot be queried. */
+/* Chunks per KV head that q4_flash_decode plans for (n_chunks itself when > 0;
+ * the default needs the current device's SM count, and a call with a short
+ * max_len uses at most ceil(max_len / 32) of them); the workspace is sized for
+ * this count.  0 for invalid arguments or when the device cannot be queried. */
 int q4_flash_decode_chunks(int n_kv_heads, int n_chunks);
 /* Workspace bytes for these sizes (0 for invalid arguments, as above). */
 size_t q4_flash_decode_workspace_bytes(int B, int n_q_heads, int n_kv_heads, int head_dim, int n_chunks);

@@ -657,6 +657,11 @@ extern "C" q4_status q4_flash_decode(const uint16_t* Q, const uint16_t* K_cache,
         sms = q4i_sm_count(nullptr);
         if (sms <= 0) return Q4_ERR_CUDA;
         C = fd_chunks(n_kv_heads, 0, sms);
+        // no more chunks than a max_len cache has at the minimum length: every chunk stays
+        // kFdMinChunk long either way (ceil(len / C) <= kFdMinChunk for len <= max_len), so the
+        // result is the same, and the combine looks at fewer chunk slots
+        const int64_t short_c = (max_len + kFdMinChunk - 1) / kFdMinChunk;
+        if (short_c < C) C = static_cast<int>(short_c);
     }
     const size_t need = fd_part_bytes(B, n_q_heads, head_dim, C) +
                         static_cast<size_t>(B) * n_q_heads * C * 2 * sizeof(float);
